@@ -1,0 +1,95 @@
+"""Calibrate the row correlation of the verify workload on the oracle.
+
+The forward_moe page reports that, on a live routing trace (top_k = 8), the
+union of the experts selected by K consecutive tokens averages
+8.00 / 13.74 / 18.76 / 23.35 at K = 1..4.  The trace and the trained router
+behind it are not available, so the verify and sweep workloads draw
+correlated rows x_t = a*s + sqrt(1-a^2)*n_t and this script picks ``a``:
+it routes seeded 4-row steps through the ORACLE's router and top-k (bf16
+router, sigmoid scoring with correction bias, E = 256, H = 4096), measures
+the mean union of the first K rows for K = 1..4, and minimises the summed
+squared relative error over K = 2..4 by a coarse scan plus golden-section
+refinement.  Output: corr_calibration.json next to this file.
+
+Run:  python tests/golden/make_corr_calibration.py
+Only oracle/ and the seeded generator are used.
+"""
+import json
+import math
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+sys.path.insert(0, ROOT)
+
+from oracle import oracle  # noqa: E402
+from routed_moe_decode_router_gb300 import synth  # noqa: E402
+
+TARGET = {1: 8.00, 2: 13.74, 3: 18.76, 4: 23.35}
+LAYERS = 4
+STEPS = 100
+
+
+def union_curve(layers, a, steps=STEPS, seed0=2500):
+    wl = synth.WORKLOADS["verify_h4096_e256"]
+    tot = np.zeros(5)
+    n = 0
+    for li, ol in enumerate(layers):
+        for st in range(steps):
+            x = synth.make_rows(wl.shape, 4, seed=seed0 + 1000 * li + st, corr=a)
+            _, ids, _ = ol.route(x)
+            for K in range(1, 5):
+                tot[K] += oracle.union(ids[:K])[0]
+            n += 1
+    return {K: tot[K] / n for K in range(1, 5)}
+
+
+def loss(curve):
+    return sum(((curve[K] - TARGET[K]) / TARGET[K]) ** 2 for K in (2, 3, 4))
+
+
+def main():
+    oracle.build()
+    wl = synth.WORKLOADS["verify_h4096_e256"]
+    layers = [oracle.OracleLayer(synth.make_layer(wl.shape, wl.seed_base + l,
+                                                  router_only=True))
+              for l in range(LAYERS)]
+    grid = np.linspace(0.50, 0.95, 10)
+    scores = [(loss(union_curve(layers, a, steps=40)), a) for a in grid]
+    _, a0 = min(scores)
+    lo, hi = max(0.0, a0 - 0.05), min(0.99, a0 + 0.05)
+    g = (math.sqrt(5) - 1) / 2
+    c, d = hi - g * (hi - lo), lo + g * (hi - lo)
+    fc, fd = loss(union_curve(layers, c)), loss(union_curve(layers, d))
+    for _ in range(8):
+        if fc < fd:
+            hi, d, fd = d, c, fc
+            c = hi - g * (hi - lo)
+            fc = loss(union_curve(layers, c))
+        else:
+            lo, c, fc = c, d, fd
+            d = lo + g * (hi - lo)
+            fd = loss(union_curve(layers, d))
+    a = round((lo + hi) / 2, 3)
+    curve = union_curve(layers, a)
+    out = {
+        "a": a,
+        "mean_union": {str(K): round(v, 3) for K, v in curve.items()},
+        "target_mean_union": {str(K): v for K, v in TARGET.items()},
+        "sample": "%d layers x %d steps of 4 rows, verify_h4096_e256 router "
+                  "(seeds %d..), activation seeds 2500 + 1000*layer + step"
+                  % (LAYERS, STEPS, wl.seed_base),
+        "source": "forward_moe page, note on partial amortisation over a "
+                  "verify's rows (live routing trace, 42 series x 406 steps)",
+    }
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                        "corr_calibration.json")
+    with open(path, "w") as f:
+        json.dump(out, f, indent=1)
+    print(json.dumps(out, indent=1))
+
+
+if __name__ == "__main__":
+    main()
