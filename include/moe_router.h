@@ -1,0 +1,226 @@
+/*
+ * moe_router.h -- C ABI of the GB300 (sm_103a) routed mixture-of-experts
+ * forward for small decode, speculative-verify and prefill sub-chunks
+ * (1..8 token rows).
+ *
+ * The operation is the routed MoE layer of page "Function forward_moe"
+ * (forward_moe(gpu, k, cfg, w, x, out, rows, ws, stream): "Routed MoE over
+ * rows rows", with the shared expert run once over all rows) and of page
+ * "metrale_model_layers/layers/moe/forward_token_major.rs"
+ * (MoeLayer::forward_token_major_decode: gate projection, batched top-k,
+ * gate+up, silu+down, weighted sum + shared-expert blend).  The union of the
+ * experts selected by all rows is built on the device by pairwise scan, as
+ * the forward_moe page's RETRACTED note describes, and every union expert's
+ * NVFP4 weights are streamed once for all the rows that selected it; the
+ * selected ids never travel to the host.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" point to GPU global memory of the current
+ *     device; "host" pointers to CPU memory.  The caller owns every buffer;
+ *     the library never allocates, frees or synchronises inside moe_route,
+ *     moe_union or moe_forward.  Work is enqueued on `stream` (a
+ *     cudaStream_t passed as void*, NULL = the legacy default stream) and
+ *     returns immediately.
+ *   - bf16 values travel as uint16_t bit patterns.
+ *   - Every argument check runs on the host before the first launch; a
+ *     refused call enqueues nothing and returns a non-zero moe_status whose
+ *     text moe_last_error() gives (per calling thread).
+ *   - A launch failure reported by the CUDA runtime returns MOE_ERR_CUDA.
+ *   - Faults the device detects (an expert id out of range, a weight pointer
+ *     that is not 16-byte aligned, a wait that ran out of time) never trap:
+ *     the kernel records a code in the workspace's status word, skips the
+ *     offending work and finishes; moe_read_device_status() returns it.
+ *
+ * NVFP4 matrix [N][K] (N outputs, K inputs, "untransposed"):
+ *   packed  uint8 [N][K/2], row-major; the low nibble holds the even input
+ *           index, each nibble an FP4 E2M1 code (sign, 2 exponent bits with
+ *           bias 1, 1 mantissa bit);
+ *   scales  uint8 [N][K/16], row-major; one FP8 E4M3 (bias 7, no infinity)
+ *           scale per 16 contiguous inputs;
+ *   scale2  fp32, one per matrix.
+ *   weight[n][k] = e2m1(code) * e4m3(scale) * scale2.
+ *   Both arrays must start on a 16-byte boundary.
+ */
+#ifndef MOE_ROUTER_H
+#define MOE_ROUTER_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#define MOE_ABI_VERSION 1
+#define MOE_MAX_ROWS 8        /* rows per call (forward_moe page, WIDENED note) */
+#define MOE_MAX_IDS 64        /* rows * top_k: one block's pairwise scan */
+#define MOE_MAX_HIDDEN 4096
+#define MOE_MAX_EXPERTS 1024
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, size out of range */
+    MOE_ERR_UNSUPPORTED = 2,    /* a configuration this path refuses */
+    MOE_ERR_WORKSPACE = 3,      /* workspace missing, too small or misaligned */
+    MOE_ERR_CUDA = 4,           /* the CUDA runtime reported an error */
+    MOE_ERR_DEVICE_STATUS = 5   /* the device recorded a fault (see below) */
+} moe_status;
+
+/* Device-side fault codes (moe_read_device_status). */
+#define MOE_DEV_OK 0
+#define MOE_DEV_BAD_EXPERT_ID 1     /* an id outside [0, num_experts) */
+#define MOE_DEV_MISALIGNED_PTR 2    /* an expert matrix not 16-byte aligned */
+#define MOE_DEV_WAIT_TIMEOUT 3      /* an on-chip wait exceeded its bound */
+
+enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
+enum { MOE_ROUTER_BF16 = 0, MOE_ROUTER_NVFP4 = 1 };
+
+/* One NVFP4 matrix whose pointers the host knows (router, shared expert). */
+typedef struct moe_nvfp4 {
+    const uint8_t *packed;   /* device, [N][K/2] */
+    const uint8_t *scales;   /* device, [N][K/16] */
+    float scale2;            /* per-tensor scale */
+} moe_nvfp4;
+
+/* Layer configuration (page "Function forward_moe": Glm5NextMlpConfig;
+ * forward_token_major.rs: hidden_size, moe_intermediate_size, num_experts,
+ * num_experts_per_tok, norm_topk_prob, routed_scaling_factor). */
+typedef struct moe_config {
+    int hidden;                  /* H: multiple of 128, 128..4096 */
+    int num_experts;             /* E: 1..1024 routed experts */
+    int router_width;            /* router output count; must equal E (wider
+                                    "zero-computation" routers are refused, as
+                                    both source pages refuse them) */
+    int top_k;                   /* k: 1..min(E, 64) */
+    int moe_inter;               /* I: multiple of 128 */
+    int shared_inter;            /* Is: multiple of 128 (ignored if no shared) */
+    int scoring;                 /* MOE_SCORING_SOFTMAX or _SIGMOID */
+    int norm_topk_prob;          /* renormalise the k weights to sum 1 */
+    float routed_scaling_factor; /* sigmoid scoring only; softmax requires 1 */
+    int router_fmt;              /* MOE_ROUTER_BF16 or MOE_ROUTER_NVFP4 */
+    int has_shared;              /* 1 = a shared expert is present */
+    int shared_gate;             /* 1 = blend sigmoid(x . shared_expert_gate),
+                                    0 = plain add of the shared expert */
+    int per_row_mode;            /* 1 = no de-duplication: every (row, slot)
+                                    pair streams its expert separately (the
+                                    token-major reference order); the output
+                                    is byte-identical to the union mode */
+} moe_config;
+
+/* Per-expert NVFP4 matrices: device arrays indexed by expert id
+ * (forward_token_major.rs: packed_ptrs / scale_ptrs / scale2_vals). */
+typedef struct moe_expert_table {
+    const uint8_t *const *packed;  /* device array [E] of device pointers */
+    const uint8_t *const *scales;  /* device array [E] of device pointers */
+    const float *scale2;           /* device array [E] */
+} moe_expert_table;
+
+typedef struct moe_weights {
+    const uint16_t *router_bf16;     /* device [E][H] bf16 (router_fmt BF16) */
+    moe_nvfp4 router_nvfp4;          /* [E][H] (router_fmt NVFP4) */
+    const float *correction_bias;    /* device [E] fp32 (sigmoid scoring) */
+    moe_expert_table gate;           /* each [I][H] */
+    moe_expert_table up;             /* each [I][H] */
+    moe_expert_table down;           /* each [H][I] */
+    moe_nvfp4 shared_gate_proj;      /* [Is][H] */
+    moe_nvfp4 shared_up_proj;        /* [Is][H] */
+    moe_nvfp4 shared_down_proj;      /* [H][Is] */
+    const uint16_t *shared_expert_gate; /* device [H] bf16 (shared_gate = 1) */
+} moe_weights;
+
+/* Result of the union step (device-resident; moe_union and
+ * moe_read_routing copy it out).  Positions p = row * top_k + slot. */
+typedef struct moe_union_table {
+    int32_t num_union;                  /* U <= min(rows * top_k, E) */
+    int32_t rows;
+    int32_t top_k;
+    int32_t per_row_mode;
+    int32_t expert[MOE_MAX_IDS];        /* union[u]: expert id, u < U */
+    uint8_t rowmask[MOE_MAX_IDS];       /* bit r: row r selected union[u] */
+    uint8_t slot2u[MOE_MAX_IDS];        /* [p]: union index of position p */
+    uint8_t uslot[MOE_MAX_IDS][MOE_MAX_ROWS]; /* [u][r]: slot of union[u] in
+                                           row r, 0xFF if r did not pick it */
+} moe_union_table;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION when built). */
+MOE_API int moe_abi_version(void);
+
+/* Text of the last refusal or error on the calling thread ("" if none). */
+MOE_API const char *moe_last_error(void);
+
+/* Host-only validation of a configuration (no CUDA call).  Returns MOE_OK or
+ * the refusal; moe_route / moe_union / moe_forward run the same checks. */
+MOE_API moe_status moe_check_config(const moe_config *cfg);
+
+/* Bytes of caller-owned device workspace the calls below need for `cfg`
+ * (routing scratch, union and pointer tables, intermediate activations,
+ * tile counters and the status word; the scratch layout starts with the
+ * top-k ids followed by the routing weights, as forward_token_major.rs lays
+ * out its scratch).  Returns 0 when the configuration is refused.  The
+ * workspace must be 256-byte aligned. */
+MOE_API size_t moe_workspace_size(const moe_config *cfg);
+
+/* Zero the workspace's counters and status word (async on `stream`).  Call
+ * once after allocating a workspace; every later call leaves the counters
+ * at zero again. */
+MOE_API moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Router + top-k for `rows` rows (forward_token_major.rs: gate projection
+ * then moe_topk_softmax_batched / moe_topk_sigmoid_batched).
+ *   x       device [rows][H] bf16, 16-byte aligned
+ *   ids     device [rows][top_k] int32, descending score, ties -> lower id
+ *   wts     device [rows][top_k] fp32 routing weights
+ *   logits  device [rows][E] fp32 router logits, or NULL */
+MOE_API moe_status moe_route(const moe_config *cfg, const moe_weights *w,
+                     const uint16_t *x, int rows, int32_t *ids, float *wts,
+                     float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/* Union of caller-given ids [rows][top_k] (device int32) by one block's
+ * pairwise scan (forward_moe page, RETRACTED note), with the device pointer
+ * table of the union experts built in the workspace.  `out` is a device
+ * moe_union_table.  `w` supplies the expert tables for the pointer table
+ * and may be NULL (no pointer table).  Ids outside [0, E) are recorded as
+ * MOE_DEV_BAD_EXPERT_ID and skipped. */
+MOE_API moe_status moe_union(const moe_config *cfg, const moe_weights *w,
+                     const int32_t *ids, int rows, moe_union_table *out,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/* The whole routed MoE layer (page "Function forward_moe": forward_moe(x,
+ * out, rows)):
+ *   out[r] = sum_{slot < k} wts[r][slot] * Expert_{ids[r][slot]}(x[r])
+ *            + g_r * Shared(x[r]),
+ *   Expert(x) = Wd (silu(Wg x) * (Wu x)), g_r = sigmoid(x[r] . gs) with
+ *   shared_gate = 1, 1 with shared_gate = 0, 0 without a shared expert.
+ *   x    device [rows][H] bf16, 16-byte aligned
+ *   out  device [rows][H] bf16, 16-byte aligned, must not overlap x
+ * `out` is the MoE output only (the residual add is the caller's).  Nothing
+ * is read back to the host, so the call can be captured in a CUDA graph. */
+MOE_API moe_status moe_forward(const moe_config *cfg, const moe_weights *w,
+                       const uint16_t *x, uint16_t *out, int rows, void *ws,
+                       size_t ws_bytes, void *stream);
+
+/* Copy the routing of the last moe_forward / moe_route on this workspace
+ * into caller buffers (async device-to-device copies on `stream`; any
+ * pointer may be NULL): ids / wts device [rows][top_k], uni a device
+ * moe_union_table (valid after moe_forward or moe_union). */
+MOE_API moe_status moe_read_routing(const moe_config *cfg, const void *ws,
+                            size_t ws_bytes, int rows, int32_t *ids,
+                            float *wts, moe_union_table *uni, void *stream);
+
+/* Synchronise `stream`, read the workspace's device status word into *code
+ * (MOE_DEV_*), and clear it.  Returns MOE_ERR_DEVICE_STATUS when the code is
+ * non-zero.  Test and diagnostics use only: it blocks the host. */
+MOE_API moe_status moe_read_device_status(void *ws, size_t ws_bytes, int *code,
+                                  void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTER_H */

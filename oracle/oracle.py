@@ -235,7 +235,7 @@ class OracleLayer:
         w.gate = C.cast(arrs["gate"], C.c_void_p)
         w.up = C.cast(arrs["up"], C.c_void_p)
         w.down = C.cast(arrs["down"], C.c_void_p)
-        if s.has_shared:
+        if s.has_shared and layer.sh_gate is not None:
             for name, field in (("sh_gate", "sh_gate"), ("sh_up", "sh_up"),
                                 ("sh_down", "sh_down")):
                 m = getattr(layer, name)

@@ -1,0 +1,420 @@
+// moe_api.cu -- host side of the C ABI declared in include/moe_router.h:
+// argument checks (all before the first launch), workspace layout, and the
+// launch sequence route -> gate+up -> down+blend, chained with programmatic
+// dependent launch on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "moe_layout.h"
+
+namespace moe {
+cudaError_t launch_route(const RouteParams &p, cudaStream_t stream);
+cudaError_t launch_union(const UnionParams &p, cudaStream_t stream);
+cudaError_t launch_gate_up(const ExpertParams &p, int grid, size_t smem, int maxc,
+                           cudaStream_t stream);
+cudaError_t launch_down(const ExpertParams &p, int grid, int W, size_t smem, int maxc,
+                        cudaStream_t stream);
+cudaError_t set_expert_smem_limits(int bytes);
+size_t gate_up_fixed_smem(int stages);
+size_t down_fixed_smem(int stages);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+thread_local char g_err[512];
+
+moe_status fail(moe_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+moe_status ok() {
+    g_err[0] = 0;
+    return MOE_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Per-device facts, looked up once.
+struct DevInfo {
+    int sms = 0;
+    int smem_optin = 0;
+    bool attrs_set = false;
+};
+std::mutex g_mu;
+DevInfo g_dev[64];
+
+moe_status device_info(DevInfo **out) {
+    int d = 0;
+    cudaError_t e = cudaGetDevice(&d);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (d < 0 || d >= 64) return fail(MOE_ERR_CUDA, "device ordinal %d out of range", d);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &di = g_dev[d];
+    if (!di.attrs_set) {
+        if ((e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, d)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        d)) != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+        if ((e = set_expert_smem_limits(di.smem_optin - 1024)) != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        di.attrs_set = true;
+    }
+    *out = &di;
+    return MOE_OK;
+}
+
+moe_status check_cfg(const moe_config *c) {
+    if (!c) return fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
+    if (c->hidden < kChunk || c->hidden > MOE_MAX_HIDDEN || c->hidden % kChunk)
+        return fail(MOE_ERR_INVALID_ARG, "hidden=%d: must be a multiple of %d in [%d, %d]",
+                    c->hidden, kChunk, kChunk, MOE_MAX_HIDDEN);
+    if (c->num_experts < 1 || c->num_experts > MOE_MAX_EXPERTS)
+        return fail(MOE_ERR_INVALID_ARG, "num_experts=%d: must be in [1, %d]", c->num_experts,
+                    MOE_MAX_EXPERTS);
+    if (c->router_width != c->num_experts)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "router_width=%d differs from num_experts=%d: zero-computation experts "
+                    "are not supported by this path",
+                    c->router_width, c->num_experts);
+    if (c->top_k < 1 || c->top_k > c->num_experts || c->top_k > MOE_MAX_IDS)
+        return fail(MOE_ERR_INVALID_ARG, "top_k=%d: must be in [1, min(num_experts, %d)]",
+                    c->top_k, MOE_MAX_IDS);
+    if (c->moe_inter < kChunk || c->moe_inter % kChunk || c->moe_inter > 4 * kConsumerWarps * kChunk)
+        return fail(MOE_ERR_INVALID_ARG, "moe_inter=%d: must be a multiple of %d in [%d, %d]",
+                    c->moe_inter, kChunk, kChunk, 4 * kConsumerWarps * kChunk);
+    if (c->has_shared != 0 && c->has_shared != 1)
+        return fail(MOE_ERR_INVALID_ARG, "has_shared must be 0 or 1");
+    if (c->has_shared &&
+        (c->shared_inter < kChunk || c->shared_inter % kChunk ||
+         c->shared_inter > 4 * kConsumerWarps * kChunk))
+        return fail(MOE_ERR_INVALID_ARG, "shared_inter=%d: must be a multiple of %d in [%d, %d]",
+                    c->shared_inter, kChunk, kChunk, 4 * kConsumerWarps * kChunk);
+    if (c->scoring != MOE_SCORING_SOFTMAX && c->scoring != MOE_SCORING_SIGMOID)
+        return fail(MOE_ERR_INVALID_ARG, "scoring=%d: must be softmax (0) or sigmoid (1)",
+                    c->scoring);
+    if (c->scoring == MOE_SCORING_SOFTMAX && c->routed_scaling_factor != 1.0f)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "routed_scaling_factor=%g with softmax scoring: the softmax top-k takes "
+                    "no scaling factor (must be 1)",
+                    (double)c->routed_scaling_factor);
+    if (!std::isfinite(c->routed_scaling_factor))
+        return fail(MOE_ERR_INVALID_ARG, "routed_scaling_factor is not finite");
+    if (c->router_fmt != MOE_ROUTER_BF16 && c->router_fmt != MOE_ROUTER_NVFP4)
+        return fail(MOE_ERR_INVALID_ARG, "router_fmt=%d: must be bf16 (0) or nvfp4 (1)",
+                    c->router_fmt);
+    if ((c->norm_topk_prob | c->shared_gate | c->per_row_mode) & ~1)
+        return fail(MOE_ERR_INVALID_ARG, "norm_topk_prob, shared_gate, per_row_mode are 0/1");
+    return MOE_OK;
+}
+
+moe_status check_rows(const moe_config *c, int rows) {
+    if (rows < 1 || rows > MOE_MAX_ROWS)
+        return fail(MOE_ERR_INVALID_ARG, "rows=%d: must be in [1, %d]", rows, MOE_MAX_ROWS);
+    if (rows * c->top_k > MOE_MAX_IDS)
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "rows*top_k=%d exceeds %d ids (one block's pairwise scan)",
+                    rows * c->top_k, MOE_MAX_IDS);
+    return MOE_OK;
+}
+
+moe_status check_ws(const moe_config *c, const void *ws, size_t ws_bytes, WsLayout *L) {
+    *L = WsLayout::make(*c);
+    if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(MOE_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+    if (ws_bytes < L->total)
+        return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, L->total);
+    return MOE_OK;
+}
+
+moe_status check_mat(const moe_nvfp4 &m, const char *name) {
+    if (!m.packed || !m.scales) return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer", name);
+    if (!aligned(m.packed, 16) || !aligned(m.scales, 16))
+        return fail(MOE_ERR_INVALID_ARG, "%s: packed/scales must be 16-byte aligned", name);
+    return MOE_OK;
+}
+
+moe_status check_table(const moe_expert_table &t, const char *name) {
+    if (!t.packed || !t.scales || !t.scale2)
+        return fail(MOE_ERR_INVALID_ARG, "%s expert table: NULL array", name);
+    if (!aligned(t.packed, 8) || !aligned(t.scales, 8) || !aligned(t.scale2, 4))
+        return fail(MOE_ERR_INVALID_ARG, "%s expert table: misaligned array", name);
+    return MOE_OK;
+}
+
+moe_status check_weights(const moe_config *c, const moe_weights *w, bool experts) {
+    moe_status s;
+    if (!w) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
+    if (c->router_fmt == MOE_ROUTER_BF16) {
+        if (!w->router_bf16 || !aligned(w->router_bf16, 16))
+            return fail(MOE_ERR_INVALID_ARG, "router_bf16: NULL or not 16-byte aligned");
+    } else if ((s = check_mat(w->router_nvfp4, "router_nvfp4")) != MOE_OK) {
+        return s;
+    }
+    if (c->scoring == MOE_SCORING_SIGMOID && (!w->correction_bias || !aligned(w->correction_bias, 4)))
+        return fail(MOE_ERR_INVALID_ARG, "sigmoid scoring needs correction_bias");
+    if (c->has_shared && c->shared_gate &&
+        (!w->shared_expert_gate || !aligned(w->shared_expert_gate, 16)))
+        return fail(MOE_ERR_INVALID_ARG, "shared_gate=1 needs a 16-byte aligned shared_expert_gate");
+    if (!experts) return MOE_OK;
+    if ((s = check_table(w->gate, "gate")) != MOE_OK) return s;
+    if ((s = check_table(w->up, "up")) != MOE_OK) return s;
+    if ((s = check_table(w->down, "down")) != MOE_OK) return s;
+    if (c->has_shared) {
+        if ((s = check_mat(w->shared_gate_proj, "shared_gate_proj")) != MOE_OK) return s;
+        if ((s = check_mat(w->shared_up_proj, "shared_up_proj")) != MOE_OK) return s;
+        if ((s = check_mat(w->shared_down_proj, "shared_down_proj")) != MOE_OK) return s;
+    }
+    return MOE_OK;
+}
+
+moe_status check_io(const void *x, const void *out, int rows, int H) {
+    if (!x || !aligned(x, 16)) return fail(MOE_ERR_INVALID_ARG, "x: NULL or not 16-byte aligned");
+    if (out) {
+        if (!aligned(out, 16)) return fail(MOE_ERR_INVALID_ARG, "out: not 16-byte aligned");
+        const char *a = static_cast<const char *>(x), *b = static_cast<const char *>(out);
+        const size_t n = (size_t)rows * H * 2;
+        if (a < b + n && b < a + n) return fail(MOE_ERR_INVALID_ARG, "x and out overlap");
+    }
+    return MOE_OK;
+}
+
+RouteParams route_params(const moe_config *c, const moe_weights *w, const uint16_t *x, int rows,
+                         const WsPtrs &wp) {
+    RouteParams p{};
+    p.H = c->hidden;
+    p.E = c->num_experts;
+    p.k = c->top_k;
+    p.rows = rows;
+    p.scoring = c->scoring;
+    p.norm = c->norm_topk_prob;
+    p.router_fmt = c->router_fmt;
+    p.has_shared = c->has_shared;
+    p.shared_gated = c->has_shared && c->shared_gate;
+    p.per_row_mode = c->per_row_mode;
+    p.rsf = c->routed_scaling_factor;
+    p.x = x;
+    p.router_bf16 = w->router_bf16;
+    p.router_fp4 = w->router_nvfp4;
+    p.bias = w->correction_bias;
+    p.sh_vec = w->shared_expert_gate;
+    p.gate = w->gate;
+    p.up = w->up;
+    p.down = w->down;
+    p.sh_gate = w->shared_gate_proj;
+    p.sh_up = w->shared_up_proj;
+    p.sh_down = w->shared_down_proj;
+    p.ws = wp;
+    return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char *moe_last_error(void) { return g_err; }
+
+moe_status moe_check_config(const moe_config *cfg) {
+    moe_status s = check_cfg(cfg);
+    return s == MOE_OK ? ok() : s;
+}
+
+size_t moe_workspace_size(const moe_config *cfg) {
+    if (check_cfg(cfg) != MOE_OK) return 0;
+    return WsLayout::make(*cfg).total;
+}
+
+moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream) {
+    if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(WsHeader))
+        return fail(MOE_ERR_WORKSPACE, "workspace NULL, misaligned or too small");
+    cudaError_t e = cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaMemsetAsync: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+moe_status moe_route(const moe_config *cfg, const moe_weights *w, const uint16_t *x, int rows,
+                     int32_t *ids, float *wts, float *logits, void *ws, size_t ws_bytes,
+                     void *stream) {
+    moe_status s;
+    WsLayout L;
+    if ((s = check_cfg(cfg)) != MOE_OK || (s = check_rows(cfg, rows)) != MOE_OK ||
+        (s = check_weights(cfg, w, false)) != MOE_OK ||
+        (s = check_io(x, nullptr, rows, cfg->hidden)) != MOE_OK ||
+        (s = check_ws(cfg, ws, ws_bytes, &L)) != MOE_OK)
+        return s;
+    if ((ids && !aligned(ids, 4)) || (wts && !aligned(wts, 4)) || (logits && !aligned(logits, 4)))
+        return fail(MOE_ERR_INVALID_ARG, "ids / wts / logits must be 4-byte aligned");
+    RouteParams p = route_params(cfg, w, x, rows, ws_ptrs(ws, L));
+    p.do_union = 0;
+    p.ids_out = ids;
+    p.wts_out = wts;
+    p.logits_out = logits;
+    cudaError_t e = launch_route(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+moe_status moe_union(const moe_config *cfg, const moe_weights *w, const int32_t *ids, int rows,
+                     moe_union_table *out, void *ws, size_t ws_bytes, void *stream) {
+    moe_status s;
+    WsLayout L;
+    if ((s = check_cfg(cfg)) != MOE_OK || (s = check_rows(cfg, rows)) != MOE_OK ||
+        (s = check_ws(cfg, ws, ws_bytes, &L)) != MOE_OK)
+        return s;
+    if (!ids || !aligned(ids, 4)) return fail(MOE_ERR_INVALID_ARG, "ids: NULL or misaligned");
+    if (out && !aligned(out, 4)) return fail(MOE_ERR_INVALID_ARG, "out: misaligned");
+    if (w && (s = check_weights(cfg, w, true)) != MOE_OK) return s;
+    UnionParams p{};
+    p.E = cfg->num_experts;
+    p.k = cfg->top_k;
+    p.rows = rows;
+    p.per_row_mode = cfg->per_row_mode;
+    p.has_tables = w != nullptr;
+    p.has_shared = cfg->has_shared;
+    p.ids = ids;
+    if (w) {
+        p.gate = w->gate;
+        p.up = w->up;
+        p.down = w->down;
+        p.sh_gate = w->shared_gate_proj;
+        p.sh_up = w->shared_up_proj;
+        p.sh_down = w->shared_down_proj;
+    }
+    p.ws = ws_ptrs(ws, L);
+    p.out = out;
+    cudaError_t e = launch_union(p, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "union launch: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
+                       uint16_t *out, int rows, void *ws, size_t ws_bytes, void *stream) {
+    moe_status s;
+    WsLayout L;
+    if ((s = check_cfg(cfg)) != MOE_OK || (s = check_rows(cfg, rows)) != MOE_OK ||
+        (s = check_weights(cfg, w, true)) != MOE_OK ||
+        (s = check_ws(cfg, ws, ws_bytes, &L)) != MOE_OK)
+        return s;
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    if ((s = check_io(x, out, rows, cfg->hidden)) != MOE_OK) return s;
+    DevInfo *di;
+    if ((s = device_info(&di)) != MOE_OK) return s;
+
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const WsPtrs wp = ws_ptrs(ws, L);
+    RouteParams rp = route_params(cfg, w, x, rows, wp);
+    rp.do_union = 1;
+    cudaError_t e = launch_route(rp, st);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+
+    ExpertParams ep{};
+    ep.H = cfg->hidden;
+    ep.I = cfg->moe_inter;
+    ep.Is = cfg->has_shared ? cfg->shared_inter : 0;
+    ep.k = cfg->top_k;
+    ep.rows = rows;
+    ep.has_shared = cfg->has_shared;
+    ep.x = x;
+    ep.out = out;
+    ep.sh_gate = w->shared_gate_proj;
+    ep.sh_up = w->shared_up_proj;
+    ep.sh_down = w->shared_down_proj;
+    ep.ws = wp;
+    const int smem_budget = di->smem_optin - 1024;
+    const int max_entries = (rows * cfg->top_k < cfg->num_experts ? rows * cfg->top_k
+                                                                   : cfg->num_experts);
+
+    // gate + up: stage = gate and up tiles (16 rows x H/2 packed + H/16 scales each)
+    {
+        const int nchunk = cfg->hidden / kChunk;
+        const int maxc = (nchunk + kConsumerWarps - 1) / kConsumerWarps;
+        ep.stage_bytes = (uint32_t)(2 * kTileRows * (cfg->hidden / 2 + cfg->hidden / 16));
+        int S = 8;
+        while (S > 2 && S * (size_t)ep.stage_bytes + gate_up_fixed_smem(S) > (size_t)smem_budget)
+            --S;
+        ep.stages = S;
+        const size_t smem = S * (size_t)ep.stage_bytes + gate_up_fixed_smem(S);
+        if (smem > (size_t)smem_budget)
+            return fail(MOE_ERR_UNSUPPORTED, "gate+up stage ring needs %zu bytes of shared memory",
+                        smem);
+        const int units = (cfg->has_shared ? ep.Is / kTileRows : 0) +
+                          max_entries * (cfg->moe_inter / kTileRows);
+        const int grid = units < di->sms ? units : di->sms;
+        e = launch_gate_up(ep, grid, smem, maxc, st);
+        if (e != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "gate+up launch: %s", cudaGetErrorString(e));
+    }
+    // down + weighted sum + blend: stage = one 16-row tile of Wd
+    {
+        const int kmax = L.inter_max;
+        const int nchunk = kmax / kChunk;
+        const int maxc = (nchunk + kConsumerWarps - 1) / kConsumerWarps;
+        const int W = (nchunk + maxc - 1) / maxc;
+        ep.stage_bytes = (uint32_t)(kTileRows * (kmax / 2 + kmax / 16));
+        int S = 16;
+        while (S > 2 && S * (size_t)ep.stage_bytes + down_fixed_smem(S) > (size_t)smem_budget)
+            --S;
+        ep.stages = S;
+        const size_t smem = S * (size_t)ep.stage_bytes + down_fixed_smem(S);
+        const int units = (cfg->has_shared ? cfg->hidden / kTileRows : 0) +
+                          max_entries * (cfg->hidden / kTileRows);
+        const int grid = units < di->sms ? units : di->sms;
+        e = launch_down(ep, grid, W, smem, maxc, st);
+        if (e != cudaSuccess)
+            return fail(MOE_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
+    }
+    return ok();
+}
+
+moe_status moe_read_routing(const moe_config *cfg, const void *ws, size_t ws_bytes, int rows,
+                            int32_t *ids, float *wts, moe_union_table *uni, void *stream) {
+    moe_status s;
+    WsLayout L;
+    if ((s = check_cfg(cfg)) != MOE_OK || (s = check_rows(cfg, rows)) != MOE_OK ||
+        (s = check_ws(cfg, ws, ws_bytes, &L)) != MOE_OK)
+        return s;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const char *b = static_cast<const char *>(ws);
+    const size_t n = (size_t)rows * cfg->top_k;
+    cudaError_t e = cudaSuccess;
+    if (ids && e == cudaSuccess)
+        e = cudaMemcpyAsync(ids, b + L.ids, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (wts && e == cudaSuccess)
+        e = cudaMemcpyAsync(wts, b + L.wts, n * 4, cudaMemcpyDeviceToDevice, st);
+    if (uni && e == cudaSuccess)
+        e = cudaMemcpyAsync(uni, b + L.uni, sizeof(moe_union_table), cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "cudaMemcpyAsync: %s", cudaGetErrorString(e));
+    return ok();
+}
+
+moe_status moe_read_device_status(void *ws, size_t ws_bytes, int *code, void *stream) {
+    if (!ws || !aligned(ws, 256) || ws_bytes < sizeof(WsHeader))
+        return fail(MOE_ERR_WORKSPACE, "workspace NULL, misaligned or too small");
+    if (!code) return fail(MOE_ERR_INVALID_ARG, "code is NULL");
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    WsHeader h;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = cudaMemcpy(&h, ws, sizeof h, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(ws, 0, 2 * sizeof(uint32_t));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+    *code = (int)h.status;
+    if (h.status)
+        return fail(MOE_ERR_DEVICE_STATUS, "device status %u (detail %u)", h.status,
+                    h.status_info);
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,144 @@
+// moe_layout.h -- workspace layout and kernel parameter blocks shared by the
+// host launch code and the kernels of the routed MoE library.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_router.h"
+
+namespace moe {
+
+constexpr int kMaxRows = MOE_MAX_ROWS;
+constexpr int kMaxIds = MOE_MAX_IDS;
+constexpr int kSharedEntry = kMaxIds;    // pointer-table slot of the shared expert
+constexpr int kEntries = kMaxIds + 1;
+constexpr int kTileRows = 16;            // output rows per work unit (MMA M)
+constexpr int kChunk = 128;              // inputs per consumer-warp chunk
+constexpr int kConsumerWarps = 8;        // gate+up kernel
+constexpr int kRouteWarps = 8;
+
+// Status word and counters at the start of the workspace (256 bytes).
+struct WsHeader {
+    uint32_t status;        // first MOE_DEV_* fault recorded (0 = none)
+    uint32_t status_info;   // detail of that fault (offending id / unit)
+    uint32_t route_ticket;  // last-block ticket of the route kernel
+    uint32_t pad[61];
+};
+static_assert(sizeof(WsHeader) == 256, "header size");
+
+// Device pointer table entry of one union expert (or the shared expert):
+// gate, up and down NVFP4 matrices.
+struct PtrEntry {
+    const uint8_t *packed[3];
+    const uint8_t *scales[3];
+    float scale2[3];
+    int32_t expert;         // -1 marks an entry the kernels must skip
+};
+static_assert(sizeof(PtrEntry) == 64, "pointer entry size");
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Byte offsets of every workspace region for one configuration.  The layout
+// is sized for MOE_MAX_ROWS rows, so one workspace serves every row count.
+struct WsLayout {
+    size_t header, tile_cnt, ids, wts, logits, gate_val, uni, ptrs, hbuf,
+        ybuf, ysbuf, total;
+    int inter_max;          // max(I, Is): row stride of the h buffer
+
+    static WsLayout make(const moe_config &c) {
+        WsLayout L{};
+        size_t o = 0;
+        L.header = o;   o = align256(o + sizeof(WsHeader));
+        L.tile_cnt = o; o = align256(o + sizeof(uint32_t) * (size_t)(c.hidden / kTileRows));
+        // forward_token_major.rs scratch order: ids, then routing weights.
+        L.ids = o;      o += sizeof(int32_t) * (size_t)kMaxIds;
+        L.wts = o;      o = align256(o + sizeof(float) * (size_t)kMaxIds);
+        L.logits = o;   o = align256(o + sizeof(float) * (size_t)kMaxRows * c.num_experts);
+        L.gate_val = o; o = align256(o + sizeof(float) * kMaxRows);
+        L.uni = o;      o = align256(o + sizeof(moe_union_table));
+        L.ptrs = o;     o = align256(o + sizeof(PtrEntry) * kEntries);
+        L.inter_max = c.moe_inter;
+        if (c.has_shared && c.shared_inter > L.inter_max) L.inter_max = c.shared_inter;
+        L.hbuf = o;     o = align256(o + 2 * (size_t)kEntries * kMaxRows * L.inter_max);
+        L.ybuf = o;     o = align256(o + sizeof(float) * (size_t)kMaxIds * c.hidden);
+        L.ysbuf = o;    o = align256(o + sizeof(float) * (size_t)kMaxRows * c.hidden);
+        L.total = o;
+        return L;
+    }
+};
+
+// Pointers into one workspace.
+struct WsPtrs {
+    WsHeader *hdr;
+    uint32_t *tile_cnt;
+    int32_t *ids;
+    float *wts;
+    float *logits;
+    float *gate_val;
+    moe_union_table *uni;
+    PtrEntry *ptrs;
+    uint16_t *hbuf;   // bf16 [kEntries][kMaxRows][inter_max]
+    float *ybuf;      // fp32 [kMaxIds][H]: position p = row * top_k + slot
+    float *ysbuf;     // fp32 [kMaxRows][H]: shared expert output
+    int inter_max;
+};
+
+inline WsPtrs ws_ptrs(void *ws, const WsLayout &L) {
+    char *b = static_cast<char *>(ws);
+    WsPtrs p;
+    p.hdr = reinterpret_cast<WsHeader *>(b + L.header);
+    p.tile_cnt = reinterpret_cast<uint32_t *>(b + L.tile_cnt);
+    p.ids = reinterpret_cast<int32_t *>(b + L.ids);
+    p.wts = reinterpret_cast<float *>(b + L.wts);
+    p.logits = reinterpret_cast<float *>(b + L.logits);
+    p.gate_val = reinterpret_cast<float *>(b + L.gate_val);
+    p.uni = reinterpret_cast<moe_union_table *>(b + L.uni);
+    p.ptrs = reinterpret_cast<PtrEntry *>(b + L.ptrs);
+    p.hbuf = reinterpret_cast<uint16_t *>(b + L.hbuf);
+    p.ybuf = reinterpret_cast<float *>(b + L.ybuf);
+    p.ysbuf = reinterpret_cast<float *>(b + L.ysbuf);
+    p.inter_max = L.inter_max;
+    return p;
+}
+
+// Parameters of the route kernel (router + top-k [+ union]).
+struct RouteParams {
+    int H, E, k, rows;
+    int scoring, norm, router_fmt, has_shared, shared_gated, per_row_mode;
+    int do_union;
+    float rsf;
+    const uint16_t *x;
+    const uint16_t *router_bf16;
+    moe_nvfp4 router_fp4;
+    const float *bias;
+    const uint16_t *sh_vec;
+    moe_expert_table gate, up, down;
+    moe_nvfp4 sh_gate, sh_up, sh_down;
+    WsPtrs ws;
+    int32_t *ids_out;       // optional copies for moe_route (may be null)
+    float *wts_out;
+    float *logits_out;
+};
+
+// Parameters of the union-only kernel (moe_union).
+struct UnionParams {
+    int E, k, rows, per_row_mode, has_tables, has_shared;
+    const int32_t *ids;
+    moe_expert_table gate, up, down;
+    moe_nvfp4 sh_gate, sh_up, sh_down;
+    WsPtrs ws;
+    moe_union_table *out;
+};
+
+// Parameters of the expert kernels (gate+up and down+blend).
+struct ExpertParams {
+    int H, I, Is, k, rows, has_shared, stages;
+    uint32_t stage_bytes;
+    const uint16_t *x;
+    uint16_t *out;
+    moe_nvfp4 sh_gate, sh_up, sh_down;   // host-known shared-expert matrices
+    WsPtrs ws;
+};
+
+}  // namespace moe

@@ -1,0 +1,170 @@
+"""PyTorch-facing wrapper of the C ABI: holds one layer's device tensors and
+their C descriptors, and calls the library on the current CUDA stream.
+PyTorch provides device memory and streams only; every step runs in the
+CUDA library.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional
+
+import torch
+
+from . import native as N
+from .synth import MoeLayerWeights, MoeShape
+
+
+def make_config(shape: MoeShape, per_row_mode: bool = False) -> N.MoeConfig:
+    return N.MoeConfig(
+        hidden=shape.hidden, num_experts=shape.num_experts,
+        router_width=shape.num_experts, top_k=shape.top_k,
+        moe_inter=shape.moe_inter, shared_inter=shape.shared_inter,
+        scoring=N.MOE_SCORING_SIGMOID if shape.scoring == "sigmoid" else N.MOE_SCORING_SOFTMAX,
+        norm_topk_prob=int(shape.norm_topk_prob),
+        routed_scaling_factor=float(shape.routed_scaling_factor),
+        router_fmt=N.MOE_ROUTER_NVFP4 if shape.router_fmt == "nvfp4" else N.MOE_ROUTER_BF16,
+        has_shared=int(shape.has_shared), shared_gate=int(shape.shared_gated),
+        per_row_mode=int(per_row_mode))
+
+
+def _ptr(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class DeviceLayer:
+    """One routed MoE layer resident on a CUDA device.
+
+    ``layer`` holds the weights (moved to ``device`` if needed).  The
+    per-expert pointer tables (device arrays of pointers, indexed by expert
+    id) are built here once."""
+
+    def __init__(self, layer: MoeLayerWeights, device="cuda"):
+        if layer.device != torch.device(device) and str(layer.device) != str(device):
+            layer = layer.to(device)
+        self.layer = layer
+        self.shape = layer.shape
+        s = self.shape
+        E = s.num_experts
+        self._tables = {}
+        w = N.MoeWeights()
+        if s.router_fmt == "nvfp4":
+            m = layer.router_nvfp4
+            w.router_nvfp4 = N.Nvfp4Desc(m.packed.data_ptr(), m.scales.data_ptr(),
+                                         float(m.scale2))
+        else:
+            w.router_bf16 = layer.router_bf16.data_ptr()
+        if layer.bias is not None:
+            w.correction_bias = layer.bias.data_ptr()
+        for name in ("gate", "up", "down"):
+            m = getattr(layer, name)
+            pk = m.packed.reshape(E, -1)
+            sc = m.scales.reshape(E, -1)
+            pk_ptrs = (pk.data_ptr() + torch.arange(E, dtype=torch.int64) *
+                       pk.stride(0)).to(device)
+            sc_ptrs = (sc.data_ptr() + torch.arange(E, dtype=torch.int64) *
+                       sc.stride(0)).to(device)
+            s2 = m.scale2.float().contiguous()
+            self._tables[name] = (pk_ptrs, sc_ptrs, s2)
+            setattr(w, name, N.ExpertTable(pk_ptrs.data_ptr(), sc_ptrs.data_ptr(),
+                                           s2.data_ptr()))
+        if s.has_shared:
+            for name, field in (("sh_gate", "shared_gate_proj"),
+                                ("sh_up", "shared_up_proj"),
+                                ("sh_down", "shared_down_proj")):
+                m = getattr(layer, name)
+                setattr(w, field, N.Nvfp4Desc(m.packed.data_ptr(), m.scales.data_ptr(),
+                                              float(m.scale2)))
+            if s.shared_gated:
+                w.shared_expert_gate = layer.sh_gate_vec.data_ptr()
+        self.weights = w
+        self.cfg = make_config(s)
+        self.cfg_per_row = make_config(s, per_row_mode=True)
+
+    def config(self, per_row_mode: bool = False) -> N.MoeConfig:
+        return self.cfg_per_row if per_row_mode else self.cfg
+
+
+class Workspace:
+    """Caller-owned device workspace for one layer shape (zeroed once)."""
+
+    def __init__(self, shape: MoeShape, device="cuda",
+                 stream: Optional[torch.cuda.Stream] = None):
+        self.nbytes = N.moe_workspace_size(make_config(shape))
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        N.moe_workspace_init(self.buf.data_ptr(), self.nbytes, _stream(stream))
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def status(self, stream=None) -> int:
+        """Synchronise and read (then clear) the device status word."""
+        return N.moe_read_device_status(self.ptr, self.nbytes, _stream(stream))
+
+
+def forward(dl: DeviceLayer, x: torch.Tensor, ws: Workspace,
+            out: Optional[torch.Tensor] = None, per_row_mode: bool = False,
+            stream=None) -> torch.Tensor:
+    """out[rows, H] (bf16) = routed MoE layer of x[rows, H] (bf16)."""
+    rows, H = x.shape
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    if out is None:
+        out = torch.empty_like(x)
+    N.moe_forward(dl.config(per_row_mode), dl.weights, x.data_ptr(), out.data_ptr(),
+                  rows, ws.ptr, ws.nbytes, _stream(stream))
+    return out
+
+
+def route(dl: DeviceLayer, x: torch.Tensor, ws: Workspace, stream=None):
+    """Router + top-k: (ids [rows, k] int32, wts [rows, k] fp32,
+    logits [rows, E] fp32)."""
+    rows = x.shape[0]
+    k, E = dl.shape.top_k, dl.shape.num_experts
+    ids = torch.empty((rows, k), dtype=torch.int32, device=x.device)
+    wts = torch.empty((rows, k), dtype=torch.float32, device=x.device)
+    logits = torch.empty((rows, E), dtype=torch.float32, device=x.device)
+    N.moe_route(dl.cfg, dl.weights, x.data_ptr(), rows, ids.data_ptr(), wts.data_ptr(),
+                logits.data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
+    return ids, wts, logits
+
+
+def _union_from_bytes(raw: torch.Tensor) -> dict:
+    t = N.UnionTable.from_buffer_copy(bytes(raw.cpu().numpy().tobytes()))
+    U = t.num_union
+    n = t.rows * t.top_k
+    return {
+        "U": U,
+        "expert": [t.expert[i] for i in range(U)],
+        "rowmask": [t.rowmask[i] for i in range(U)],
+        "slot2u": [t.slot2u[i] for i in range(n)],
+        "uslot": [[t.uslot[u][r] for r in range(N.MOE_MAX_ROWS)] for u in range(U)],
+        "rows": t.rows, "top_k": t.top_k, "per_row_mode": t.per_row_mode,
+    }
+
+
+def union(dl: Optional[DeviceLayer], cfg: N.MoeConfig, ids: torch.Tensor,
+          ws: Workspace, stream=None) -> dict:
+    """Union of ids [rows, k] (device int32) built on the device."""
+    rows = ids.shape[0]
+    raw = torch.empty(C.sizeof(N.UnionTable), dtype=torch.uint8, device=ids.device)
+    N.moe_union(cfg, dl.weights if dl is not None else None, ids.data_ptr(), rows,
+                raw.data_ptr(), ws.ptr, ws.nbytes, _stream(stream))
+    return _union_from_bytes(raw)
+
+
+def read_routing(dl: DeviceLayer, ws: Workspace, rows: int, per_row_mode=False,
+                 stream=None):
+    """(ids, wts, union dict) of the last call on this workspace."""
+    k = dl.shape.top_k
+    dev = ws.buf.device
+    ids = torch.empty((rows, k), dtype=torch.int32, device=dev)
+    wts = torch.empty((rows, k), dtype=torch.float32, device=dev)
+    raw = torch.empty(C.sizeof(N.UnionTable), dtype=torch.uint8, device=dev)
+    N.moe_read_routing(dl.config(per_row_mode), ws.ptr, ws.nbytes, rows, ids.data_ptr(),
+                       wts.data_ptr(), raw.data_ptr(), _stream(stream))
+    return ids, wts, _union_from_bytes(raw)

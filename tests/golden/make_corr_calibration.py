@@ -54,7 +54,8 @@ def main():
     oracle.build()
     wl = synth.WORKLOADS["verify_h4096_e256"]
     layers = [oracle.OracleLayer(synth.make_layer(wl.shape, wl.seed_base + l,
-                                                  router_only=True))
+                                                  router_only=True),
+                                  experts=())
               for l in range(LAYERS)]
     grid = np.linspace(0.50, 0.95, 10)
     scores = [(loss(union_curve(layers, a, steps=40)), a) for a in grid]

@@ -1,0 +1,190 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads and
+exports every entry point the header declares, the ctypes structures match
+the C layout, and every refusal happens on the host before any launch."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+from routed_moe_decode_router_gb300 import build as B
+from routed_moe_decode_router_gb300 import layer as L
+from routed_moe_decode_router_gb300 import native as N
+from routed_moe_decode_router_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_router.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return N.lib()
+
+
+def header_functions():
+    text = open(HEADER).read()
+    return re.findall(r"MOE_API\s+[\w\s\*]+?\b(moe_\w+)\s*\(", text)
+
+
+def test_library_exports_every_declared_function(lib):
+    declared = header_functions()
+    assert len(declared) == 10
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(moe_\w+)", out))
+    assert set(declared) == exported
+    assert set(declared) == set(N.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_abi_version(lib):
+    assert N.moe_abi_version() == 1
+
+
+def test_ctypes_layout_matches_c_header(tmp_path):
+    structs = {"moe_nvfp4": N.Nvfp4Desc, "moe_config": N.MoeConfig,
+               "moe_expert_table": N.ExpertTable, "moe_weights": N.MoeWeights,
+               "moe_union_table": N.UnionTable}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe_router.h"',
+             'int main(void) {']
+    for cname, py in structs.items():
+        lines.append('printf("%s %%zu\\n", sizeof(%s));' % (cname, cname))
+        for fname, _ in py._fields_:
+            lines.append('printf("%s.%s %%zu\\n", offsetof(%s, %s));'
+                         % (cname, fname, cname, fname))
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], capture_output=True,
+                                                  text=True, check=True).stdout.splitlines())
+    for cname, py in structs.items():
+        assert int(got[cname]) == C.sizeof(py), cname
+        for fname, _ in py._fields_:
+            assert int(got["%s.%s" % (cname, fname)]) == getattr(py, fname).offset, fname
+
+
+def good_cfg(**kw):
+    c = L.make_config(synth.WORKLOADS["tiny_h256_e16"].shape)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("num_experts", 0, N.MoeError),
+    ("router_width", 17, N.MoeError),
+    ("hidden", 200, N.MoeError),
+    ("hidden", 8192, N.MoeError),
+    ("top_k", 0, N.MoeError),
+    ("top_k", 17, N.MoeError),
+    ("moe_inter", 96, N.MoeError),
+    ("shared_inter", 64, N.MoeError),
+    ("routed_scaling_factor", 2.5, N.MoeError),
+    ("scoring", 7, N.MoeError),
+    ("router_fmt", 3, N.MoeError),
+    ("per_row_mode", 2, N.MoeError),
+])
+def test_config_refusals(lib, field, value, status):
+    cfg = good_cfg(**{field: value})
+    with pytest.raises(status):
+        N.moe_check_config(cfg)
+    assert N.lib().moe_workspace_size(C.byref(cfg)) == 0
+
+
+def test_zero_computation_router_refused_as_unsupported(lib):
+    cfg = good_cfg(router_width=20)
+    with pytest.raises(N.MoeError) as ei:
+        N.moe_check_config(cfg)
+    assert ei.value.status == 2
+    assert "zero-computation" in str(ei.value)
+
+
+def test_sigmoid_accepts_scaling_factor(lib):
+    N.moe_check_config(good_cfg(scoring=1, routed_scaling_factor=2.5))
+
+
+def test_workspace_size_independent_of_rows_and_positive(lib):
+    for name, wl in synth.WORKLOADS.items():
+        n = N.moe_workspace_size(L.make_config(wl.shape))
+        assert n > 0 and n % 256 == 0, name
+
+
+FAKE = 0x10000   # never dereferenced: every check below fails on the host
+
+
+def fake_weights():
+    w = N.MoeWeights()
+    w.router_bf16 = FAKE
+    tab = N.ExpertTable(FAKE, FAKE, FAKE)
+    w.gate = w.up = w.down = tab
+    d = N.Nvfp4Desc(FAKE, FAKE, 1.0)
+    w.shared_gate_proj = w.shared_up_proj = w.shared_down_proj = d
+    w.shared_expert_gate = FAKE
+    return w
+
+
+@pytest.mark.parametrize("case", ["rows0", "rows9", "ids65", "x_null", "overlap",
+                                  "ws_small", "ws_misaligned", "out_null",
+                                  "x_misaligned", "shared_misaligned", "bias_missing"])
+def test_forward_refusals_on_host(lib, case):
+    cfg = good_cfg()
+    w = fake_weights()
+    need = N.moe_workspace_size(cfg)
+    x, out, rows, ws, nbytes = 0x200000, 0x400000, 2, 0x800000, need
+    if case == "rows0":
+        rows = 0
+    elif case == "rows9":
+        rows = 9
+    elif case == "ids65":
+        cfg = good_cfg(top_k=16, num_experts=16, router_width=16)
+        rows = 5
+    elif case == "x_null":
+        x = 0
+    elif case == "overlap":
+        out = x + 256
+    elif case == "ws_small":
+        nbytes = need - 1
+    elif case == "ws_misaligned":
+        ws += 16
+    elif case == "out_null":
+        out = 0
+    elif case == "x_misaligned":
+        x += 2
+    elif case == "shared_misaligned":
+        w.shared_down_proj = N.Nvfp4Desc(FAKE + 8, FAKE, 1.0)
+    elif case == "bias_missing":
+        cfg = good_cfg(scoring=1, routed_scaling_factor=2.5)
+        nbytes = N.moe_workspace_size(cfg)
+    with pytest.raises(N.MoeError) as ei:
+        N.moe_forward(cfg, w, x, out, rows, ws, nbytes, 0)
+    assert ei.value.status in (1, 2, 3)
+    assert N.lib().moe_last_error().decode() != ""
+
+
+def test_route_and_union_refusals_on_host(lib):
+    cfg = good_cfg()
+    w = fake_weights()
+    need = N.moe_workspace_size(cfg)
+    with pytest.raises(N.MoeError):
+        N.moe_route(cfg, w, 0x200000, 0, 0, 0, 0, 0x800000, need, 0)
+    with pytest.raises(N.MoeError):
+        N.moe_route(cfg, w, 0x200000, 1, 0x1002, 0, 0, 0x800000, need, 0)
+    with pytest.raises(N.MoeError):
+        N.moe_union(cfg, None, 0, 1, 0, 0x800000, need, 0)
+    with pytest.raises(N.MoeError):
+        N.moe_union(cfg, None, 0x1000, 17, 0, 0x800000, need, 0)
+    with pytest.raises(N.MoeError):
+        N.moe_read_routing(cfg, 0x800001, need, 1, 0, 0, 0, 0)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(N, "_lib", None)
+    monkeypatch.setattr(N, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        N.lib()
