@@ -1,0 +1,498 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE layer forward on GB300.
+
+Metric: microseconds per routed-MoE layer-step (lower is better) and the
+weight bandwidth it implies against the measured HBM peak.  One step is one
+pass of every layer of the workload (router, top-k, union, expert sweep,
+blend) over one batch of `rows` token rows, replayed from one CUDA graph;
+every layer streams its own distinct weights, so each step touches far more
+bytes than the 129 MB L2 and no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--rows R] [--layers L] [--impl ours|reference]
+
+N > 1 runs as one process per GPU under torch.distributed.run; every rank
+runs an independent replica of the workload (the layer has no exchange step
+on one GPU), the timed region is bracketed by barriers and the slowest rank's
+time is reported.  --impl reference times the CPU oracle on the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs per routed-MoE layer-step & weight GB/s vs GB300 HBM peak, rows=1..8"
+UNIT = "us/layer-step"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas: barrier and max over ranks only)
+# ---------------------------------------------------------------------------
+
+def dist_init(device_type: str = "cuda"):
+    """(rank, world, local_rank); initialises the process group when the
+    launcher set WORLD_SIZE > 1."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world <= 1:
+        return 0, 1, 0
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    if device_type == "cuda":
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        dist.init_process_group("gloo")
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(v: float, device_type: str = "cuda") -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return v
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if device_type == "cuda" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_us_per_unit(max_elapsed_ms: float, units_per_rank: int, world: int) -> float:
+    """Whole-job microseconds per unit: every rank processed units_per_rank
+    units within the slowest rank's time."""
+    return max_elapsed_ms * 1000.0 / (units_per_rank * world)
+
+
+# ---------------------------------------------------------------------------
+# Bytes
+# ---------------------------------------------------------------------------
+
+def nvfp4_bytes(n: int, k: int) -> int:
+    return n * k // 2 + n * k // 16
+
+
+def layer_bytes(shape, rows: int, U: int) -> int:
+    """Algorithmic bytes of one layer-step: every union expert's gate, up and
+    down weights and scales once (+3 fp32 scale2), the shared expert, the
+    router, the correction bias, the shared-expert gate vector, x and out."""
+    H, E, I, Is = shape.hidden, shape.num_experts, shape.moe_inter, shape.shared_inter
+    b = U * (3 * nvfp4_bytes(I, H) + 12)
+    if shape.has_shared:
+        b += 3 * nvfp4_bytes(Is, H) + 12
+        if shape.shared_gated:
+            b += H * 2
+    b += E * H * 2 if shape.router_fmt == "bf16" else nvfp4_bytes(E, H) + 4
+    if shape.scoring == "sigmoid":
+        b += E * 4
+    b += 2 * rows * H * 2
+    return b
+
+
+def gate_up_bytes(shape, rows: int, U: int, row_counts) -> int:
+    """Algorithmic bytes of one gate+up launch: the gate and up weights and
+    scales of every union expert and the shared expert, x, and the h rows it
+    writes (one per (entry, row) pair)."""
+    H, I, Is = shape.hidden, shape.moe_inter, shape.shared_inter
+    b = U * 2 * nvfp4_bytes(I, H) + rows * H * 2 + sum(row_counts) * I * 2
+    if shape.has_shared:
+        b += 2 * nvfp4_bytes(Is, H) + rows * Is * 2
+    return b
+
+
+# ---------------------------------------------------------------------------
+# Peaks, clocks, committed ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    d = os.path.join(ROOT, "routed_moe_decode_router_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str, rows: int):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary under
+    profiles/, if it was taken on the current kernel sources (else None)."""
+    src = kernel_source_hash()
+    pat = re.compile(r"bench-traffic:\s*kernel=(\S+)\s+workload=(\S+)\s+rows=(\d+)\s+"
+                     r"bytes_per_launch=(\d+)\s+src=(\w+)")
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for line in f:
+                m = pat.search(line)
+                if (m and m.group(1) == kernel and m.group(2) == workload
+                        and int(m.group(3)) == rows and m.group(5) == src):
+                    return int(m.group(4))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# Workload
+# ---------------------------------------------------------------------------
+
+def build_workload(name, rows, n_layers, device):
+    import torch
+    from routed_moe_decode_router_gb300 import layer as L
+    from routed_moe_decode_router_gb300 import synth
+    wl = synth.WORKLOADS[name]
+    shape = wl.shape
+    layers = [L.DeviceLayer(synth.make_layer(shape, wl.seed_base + l, device=device),
+                            device=device) for l in range(n_layers)]
+    xbuf = torch.empty((n_layers, rows, shape.hidden), dtype=torch.bfloat16, device=device)
+    for l in range(n_layers):
+        xbuf[l] = synth.make_rows(shape, rows, seed=wl.seed_base + 500 + l, device=device,
+                                  corr=wl.corr)
+    outbuf = torch.empty_like(xbuf)
+    return wl, shape, layers, xbuf, outbuf
+
+
+def workload_config(wl, shape, rows, n_layers, extra=None):
+    c = {"workload": wl.name, "rows": rows, "layers": n_layers, "hidden": shape.hidden,
+         "num_experts": shape.num_experts, "top_k": shape.top_k,
+         "moe_inter": shape.moe_inter, "shared_inter": shape.shared_inter,
+         "scoring": shape.scoring, "router": shape.router_fmt,
+         "activations": "independent N(0,1)" if wl.corr is None
+         else "correlated rows, a=%.3f" % wl.corr}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def cpu_baseline(layers, xbuf, rows, sample_s, nthreads):
+    """The oracle as it stands on the host cores: whole layer forwards of
+    the same workload, layer after layer, until `sample_s` seconds of oracle
+    time have been spent (setup copies of the selected experts untimed)."""
+    from oracle import oracle
+    oracle.build()
+    spent, n, used = 0.0, 0, 1
+    for l, dl in enumerate(layers):
+        x = xbuf[l].cpu()
+        _, ids, _ = oracle.OracleLayer(dl.layer, experts=()).route(x)
+        ol = oracle.OracleLayer(dl.layer, experts=set(int(v) for v in ids.ravel()))
+        t0 = time.perf_counter()
+        ol.forward(x, nthreads=nthreads)
+        spent += time.perf_counter() - t0
+        n += 1
+        tasks = rows * (dl.shape.top_k + (1 if dl.shape.has_shared else 0))
+        used = max(used, min(nthreads, tasks))
+        if spent >= sample_s:
+            break
+    return {"value": spent / n * 1e6, "unit": UNIT, "cores": used, "kind": "oracle",
+            "sample": "%d of the workload's layers, %d row(s) each, whole-layer oracle "
+                      "forwards on %d host threads" % (n, rows, used)}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    from routed_moe_decode_router_gb300 import layer as L
+    from routed_moe_decode_router_gb300 import native as N
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from routed_moe_decode_router_gb300 import synth
+    wl0 = synth.WORKLOADS[args.workload]
+    rows = args.rows or max(wl0.rows)
+    n_layers = args.layers or wl0.layers
+    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev)
+    ws = L.Workspace(shape, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    # routing of every layer (eager, untimed): union sizes for the byte counts
+    U, rowcnt = [], []
+    with torch.cuda.stream(stream):
+        for l, dl in enumerate(layers):
+            L.forward(dl, xbuf[l], ws, out=outbuf[l])
+            _, _, uni = L.read_routing(dl, ws, rows)
+            U.append(uni["U"])
+            rowcnt.append([bin(m).count("1") for m in uni["rowmask"]])
+    stream.synchronize()
+    if ws.status() != 0:
+        raise RuntimeError("device status set during setup")
+
+    # one CUDA graph over all layers
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for l, dl in enumerate(layers):
+            L.forward(dl, xbuf[l], ws, out=outbuf[l])
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        g.replay()
+    ev1.record()
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    elapsed = ev0.elapsed_time(ev1)
+    max_elapsed = max_over_ranks(elapsed)
+    value = aggregate_us_per_unit(max_elapsed, args.steps * n_layers, world)
+    ms_per_step = max_elapsed / args.steps
+
+    # per-kernel timing pass: the same layers, events around each launch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in layers]
+    dur = {"route": 0.0, "gate_up": 0.0, "down": 0.0}
+    prof_steps = max(1, min(args.steps, 20))
+    with torch.cuda.stream(stream):
+        for _ in range(prof_steps):
+            for l, dl in enumerate(layers):
+                N.moe_forward_timed(dl.cfg, dl.weights, xbuf[l].data_ptr(),
+                                    outbuf[l].data_ptr(), rows, ws.ptr, ws.nbytes,
+                                    stream.cuda_stream, [e.cuda_event for e in evs[l]])
+            stream.synchronize()
+            for l in range(n_layers):
+                e = evs[l]
+                dur["route"] += e[0].elapsed_time(e[1])
+                dur["gate_up"] += e[1].elapsed_time(e[2])
+                dur["down"] += e[2].elapsed_time(e[3])
+    launches = prof_steps * n_layers
+    gu_bytes = sum(gate_up_bytes(shape, rows, U[l], rowcnt[l]) for l in range(n_layers))
+    gu_ms = dur["gate_up"] / launches
+    peak, peak_kind = hbm_peak()
+    achieved = gu_bytes / n_layers / (gu_ms * 1e-3) / 1e9
+    traffic = committed_traffic("moe_gate_up_kernel", args.workload, rows)
+
+    # end to end through the public API with host buffers
+    x_host = xbuf.cpu().pin_memory()
+    out_host = torch.empty(outbuf.shape, dtype=outbuf.dtype).pin_memory()
+    e2e_steps = max(1, min(args.steps, 200))
+    torch.cuda.synchronize()
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(e2e_steps):
+        xbuf.copy_(x_host, non_blocking=True)
+        g.replay()
+        out_host.copy_(outbuf, non_blocking=True)
+    t1.record()
+    t1.synchronize()
+    e2e_ms = max_over_ranks(t0.elapsed_time(t1))
+    e2e_value = aggregate_us_per_unit(e2e_ms, e2e_steps * n_layers, world)
+    if ws.status() != 0:
+        raise RuntimeError("device status set during the timed region")
+
+    step_bytes = sum(layer_bytes(shape, rows, u) for u in U)
+    layer_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16 mma / f32 accumulate (nvfp4 weights, bf16 activations)",
+        "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, bf16 activations)",
+        "config": workload_config(wl, shape, rows, n_layers, {
+            "union_mean": round(sum(U) / len(U), 3),
+            "l2": "no flush: each step streams %.2f GB of distinct weights (L2 129 MB)"
+                  % (step_bytes / 1e9),
+            "graph": "one CUDA graph of %d layers x 3 PDL-chained kernels" % n_layers,
+            "parallelism": "replicas" if world > 1 else "single GPU"}),
+        "weight_gbs": round(layer_gbs, 1),
+        "weight_frac_of_peak": round(layer_gbs / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "moe_gate_up_kernel",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": peak_kind,
+                     "kernel_ms": round(gu_ms, 5),
+                     "kernel_share": {k: round(v / sum(dur.values()), 4)
+                                      for k, v in dur.items()}},
+        "e2e": {"value": round(e2e_value, 4), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_host.numel() * 2),
+                "d2h_bytes_per_step": int(out_host.numel() * 2)},
+        "gpu_launches": 3 * n_layers * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(layers, xbuf, rows, args.cpu_sample_s,
+                                            os.cpu_count() or 1)
+    return line
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle timed on the host cores on the same workload: each
+    step is one whole layer forward (the layers in turn)."""
+    if rank != 0:
+        return None
+    import torch
+    from oracle import oracle
+    from routed_moe_decode_router_gb300 import synth
+    oracle.build()
+    wl = synth.WORKLOADS[args.workload]
+    shape = wl.shape
+    rows = args.rows or max(wl.rows)
+    n_layers = args.layers or wl.layers
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    nthreads = os.cpu_count() or 1
+    budget_s = args.reference_budget_s
+    need = min(n_layers, args.steps + args.warmup)
+    prepared = []
+    for l in range(need):
+        weights = synth.make_layer(shape, wl.seed_base + l, device=device)
+        x = synth.make_rows(shape, rows, seed=wl.seed_base + 500 + l, device=device,
+                            corr=wl.corr).cpu()
+        _, ids, _ = oracle.OracleLayer(weights, experts=()).route(x)
+        prepared.append((oracle.OracleLayer(weights, experts=set(int(v) for v in ids.ravel())),
+                         x))
+        del weights
+    for i in range(args.warmup):
+        ol, x = prepared[i % len(prepared)]
+        ol.forward(x, nthreads=nthreads)
+    times = []
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        ol, x = prepared[(args.warmup + i) % len(prepared)]
+        t0 = time.perf_counter()
+        ol.forward(x, nthreads=nthreads)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    value = sum(times) / len(times) * 1e6
+    tasks = rows * (shape.top_k + (1 if shape.has_shared else 0))
+    cores = min(nthreads, tasks)
+    sample = ("%d timed whole-layer oracle forwards (%d row(s), %d distinct layers)"
+              % (len(times), rows, len(prepared)))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": UNIT,
+        "n_gpus": world, "steps": len(times), "steps_requested": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(value / 1000.0, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, bf16 activations)",
+        "config": workload_config(wl, shape, rows, n_layers),
+        "cpu_baseline": {"value": round(value, 2), "unit": UNIT, "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_h2048_e128")
+    ap.add_argument("--rows", type=int, default=None)
+    ap.add_argument("--layers", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    ap.add_argument("--reference-budget-s", type=float, default=150.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world_env = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 and world_env != args.gpus:
+        ap.error("--gpus %d needs torch.distributed.run with %d processes"
+                 % (args.gpus, args.gpus))
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, rank, world_env)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    rank, world, local = dist_init("cuda")
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    barrier()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -300,8 +300,11 @@ moe_status moe_union(const moe_config *cfg, const moe_weights *w, const int32_t 
     return ok();
 }
 
-moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
-                       uint16_t *out, int rows, void *ws, size_t ws_bytes, void *stream) {
+}  // extern "C"
+
+static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
+                               const uint16_t *x, uint16_t *out, int rows, void *ws,
+                               size_t ws_bytes, void *stream, void *const *ev) {
     moe_status s;
     WsLayout L;
     if ((s = check_cfg(cfg)) != MOE_OK || (s = check_rows(cfg, rows)) != MOE_OK ||
@@ -317,7 +320,14 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16
     const WsPtrs wp = ws_ptrs(ws, L);
     RouteParams rp = route_params(cfg, w, x, rows, wp);
     rp.do_union = 1;
-    cudaError_t e = launch_route(rp, st);
+    cudaError_t e = cudaSuccess;
+    auto mark = [&](int i) {
+        if (ev && e == cudaSuccess) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    };
+    mark(0);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "event record: %s", cudaGetErrorString(e));
+    e = launch_route(rp, st);
+    mark(1);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
 
     ExpertParams ep{};
@@ -354,6 +364,7 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16
                           max_entries * (cfg->moe_inter / kTileRows);
         const int grid = units < di->sms ? units : di->sms;
         e = launch_gate_up(ep, grid, smem, maxc, st);
+        mark(2);
         if (e != cudaSuccess)
             return fail(MOE_ERR_CUDA, "gate+up launch: %s", cudaGetErrorString(e));
     }
@@ -373,10 +384,26 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16
                           max_entries * (cfg->hidden / kTileRows);
         const int grid = units < di->sms ? units : di->sms;
         e = launch_down(ep, grid, W, smem, maxc, st);
+        mark(3);
         if (e != cudaSuccess)
             return fail(MOE_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
     }
     return ok();
+}
+
+extern "C" {
+
+moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
+                       uint16_t *out, int rows, void *ws, size_t ws_bytes, void *stream) {
+    return forward_impl(cfg, w, x, out, rows, ws, ws_bytes, stream, nullptr);
+}
+
+moe_status moe_forward_timed(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
+                             uint16_t *out, int rows, void *ws, size_t ws_bytes, void *stream,
+                             void *const ev[4]) {
+    if (!ev || !ev[0] || !ev[1] || !ev[2] || !ev[3])
+        return fail(MOE_ERR_INVALID_ARG, "four events are required");
+    return forward_impl(cfg, w, x, out, rows, ws, ws_bytes, stream, ev);
 }
 
 moe_status moe_read_routing(const moe_config *cfg, const void *ws, size_t ws_bytes, int rows,

@@ -70,7 +70,8 @@ class UnionTable(C.Structure):
 
 EXPORTS = ("moe_abi_version", "moe_last_error", "moe_check_config",
            "moe_workspace_size", "moe_workspace_init", "moe_route", "moe_union",
-           "moe_forward", "moe_read_routing", "moe_read_device_status")
+           "moe_forward", "moe_forward_timed", "moe_read_routing",
+           "moe_read_device_status")
 
 _lib = None
 _lock = threading.Lock()
@@ -105,6 +106,8 @@ def lib():
                                 vp, vp, sz, vp]
         L.moe_forward.argtypes = [C.POINTER(MoeConfig), C.POINTER(MoeWeights), vp,
                                   vp, i, vp, sz, vp]
+        L.moe_forward_timed.argtypes = [C.POINTER(MoeConfig), C.POINTER(MoeWeights),
+                                        vp, vp, i, vp, sz, vp, C.POINTER(vp)]
         L.moe_read_routing.argtypes = [C.POINTER(MoeConfig), vp, sz, i, vp, vp,
                                        vp, vp]
         L.moe_read_device_status.argtypes = [vp, sz, C.POINTER(C.c_int), vp]
@@ -159,6 +162,14 @@ def moe_forward(cfg, w, x: int, out: int, rows: int, ws: int, ws_bytes: int,
                 stream: int = 0):
     _check(lib().moe_forward(C.byref(cfg), C.byref(w), x, out, rows, ws,
                              ws_bytes, stream))
+
+
+def moe_forward_timed(cfg, w, x: int, out: int, rows: int, ws: int,
+                      ws_bytes: int, stream: int, events):
+    """events: four cudaEvent_t handles (ints)."""
+    arr = (C.c_void_p * 4)(*events)
+    _check(lib().moe_forward_timed(C.byref(cfg), C.byref(w), x, out, rows, ws,
+                                   ws_bytes, stream, arr))
 
 
 def moe_read_routing(cfg, ws: int, ws_bytes: int, rows: int, ids: int,
