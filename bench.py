@@ -328,6 +328,10 @@ def run_ours(args, rank, world, local):
 
     # per-kernel timing pass: the same layers, events around each launch
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in layers]
+    for row in evs:                  # torch creates the CUDA event on first record
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
     dur = {"route": 0.0, "gate_up": 0.0, "down": 0.0}
     prof_steps = max(1, min(args.steps, 20))
     with torch.cuda.stream(stream):
