@@ -216,6 +216,33 @@ MOE_API moe_status moe_forward_timed(const moe_config *cfg, const moe_weights *w
                                      void *ws, size_t ws_bytes, void *stream,
                                      void *const ev[4]);
 
+/* Bytes of the library-owned device workspace behind moe_forward_static;
+ * it covers every configuration moe_check_config accepts (at most about
+ * 5.3 MB at hidden 4096, 1024 experts, intermediate 4096). */
+#define MOE_STATIC_WORKSPACE_BYTES (6u << 20)
+
+/* moe_forward for callers that cannot allocate device memory themselves --
+ * for example a plug-in running inside a host framework that owns every
+ * device allocation through its own pool and forbids side allocations, or a
+ * latency-critical path that must never enter the CUDA allocator.  The
+ * source pages have no counterpart to this entry point.
+ *
+ * Same arguments and result as moe_forward, minus the workspace: the scratch
+ * lives in one file-scope device array of MOE_STATIC_WORKSPACE_BYTES, which
+ * every GPU that loads the library holds until the process exits.  The call
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library
+ * routine).  The first call on each device looks up the array's device
+ * address; make that first call before any stream capture.  Every call
+ * clears the array's counters and status word on `stream`, then runs the
+ * layer.  All calls share the one array, so calls that overlap on the GPU
+ * (different streams, or host threads without ordering) race and must be
+ * serialised by the caller.  Device fault codes recorded by this path are
+ * cleared by the next call and are not reported.  A configuration whose
+ * workspace would exceed the array is refused with MOE_ERR_WORKSPACE. */
+MOE_API moe_status moe_forward_static(const moe_config *cfg, const moe_weights *w,
+                                      const uint16_t *x, uint16_t *out, int rows,
+                                      void *stream);
+
 /* Copy the routing of the last moe_forward / moe_route on this workspace
  * into caller buffers (async device-to-device copies on `stream`; any
  * pointer may be NULL): ids / wts device [rows][top_k], uni a device

@@ -221,6 +221,12 @@ RouteParams route_params(const moe_config *c, const moe_weights *w, const uint16
 
 }  // namespace
 
+namespace moe {
+// Record a refusal or error for moe_last_error() from another translation
+// unit of the library.
+moe_status set_error(moe_status s, const char *msg) { return fail(s, "%s", msg); }
+}  // namespace moe
+
 extern "C" {
 
 int moe_abi_version(void) { return MOE_ABI_VERSION; }

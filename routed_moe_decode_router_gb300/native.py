@@ -71,7 +71,7 @@ class UnionTable(C.Structure):
 EXPORTS = ("moe_abi_version", "moe_last_error", "moe_check_config",
            "moe_workspace_size", "moe_workspace_init", "moe_route", "moe_union",
            "moe_forward", "moe_forward_timed", "moe_read_routing",
-           "moe_read_device_status")
+           "moe_read_device_status", "moe_forward_static")
 
 _lib = None
 _lock = threading.Lock()
@@ -111,6 +111,8 @@ def lib():
         L.moe_read_routing.argtypes = [C.POINTER(MoeConfig), vp, sz, i, vp, vp,
                                        vp, vp]
         L.moe_read_device_status.argtypes = [vp, sz, C.POINTER(C.c_int), vp]
+        L.moe_forward_static.argtypes = [C.POINTER(MoeConfig), C.POINTER(MoeWeights),
+                                         vp, vp, i, vp]
         for name in EXPORTS[2:]:
             if name != "moe_workspace_size":
                 getattr(L, name).restype = i
@@ -176,6 +178,12 @@ def moe_read_routing(cfg, ws: int, ws_bytes: int, rows: int, ids: int,
                      wts: int, uni: int, stream: int = 0):
     _check(lib().moe_read_routing(C.byref(cfg), ws, ws_bytes, rows, ids, wts,
                                   uni, stream))
+
+
+def moe_forward_static(cfg, w, x: int, out: int, rows: int, stream: int = 0):
+    """moe_forward with the library's own static device workspace (for
+    callers that cannot allocate device memory; see the header)."""
+    _check(lib().moe_forward_static(C.byref(cfg), C.byref(w), x, out, rows, stream))
 
 
 def moe_read_device_status(ws: int, ws_bytes: int, stream: int = 0) -> int:

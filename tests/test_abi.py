@@ -30,7 +30,7 @@ def header_functions():
 
 def test_library_exports_every_declared_function(lib):
     declared = header_functions()
-    assert len(declared) == 11
+    assert len(declared) == 12
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(moe_\w+)", out))
