@@ -108,17 +108,6 @@ def layer_bytes(shape, rows: int, U: int) -> int:
     return b
 
 
-def gate_up_bytes(shape, rows: int, U: int, row_counts) -> int:
-    """Algorithmic bytes of one gate+up launch: the gate and up weights and
-    scales of every union expert and the shared expert, x, and the h rows it
-    writes (one per (entry, row) pair)."""
-    H, I, Is = shape.hidden, shape.moe_inter, shape.shared_inter
-    b = U * 2 * nvfp4_bytes(I, H) + rows * H * 2 + sum(row_counts) * I * 2
-    if shape.has_shared:
-        b += 2 * nvfp4_bytes(Is, H) + rows * Is * 2
-    return b
-
-
 # ---------------------------------------------------------------------------
 # Peaks, clocks, committed ncu traffic
 # ---------------------------------------------------------------------------
@@ -285,13 +274,12 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device=dev)
 
     # routing of every layer (eager, untimed): union sizes for the byte counts
-    U, rowcnt = [], []
+    U = []
     with torch.cuda.stream(stream):
         for l, dl in enumerate(layers):
             L.forward(dl, xbuf[l], ws, out=outbuf[l])
             _, _, uni = L.read_routing(dl, ws, rows)
             U.append(uni["U"])
-            rowcnt.append([bin(m).count("1") for m in uni["rowmask"]])
     stream.synchronize()
     if ws.status() != 0:
         raise RuntimeError("device status set during setup")
@@ -326,13 +314,13 @@ def run_ours(args, rank, world, local):
     value = aggregate_us_per_unit(max_elapsed, args.steps * n_layers, world)
     ms_per_step = max_elapsed / args.steps
 
-    # per-kernel timing pass: the same layers, events around each launch
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in layers]
+    # kernel timing pass: the same layers, events around each layer kernel
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in layers]
     for row in evs:                  # torch creates the CUDA event on first record
         for e in row:
             e.record(stream)
     stream.synchronize()
-    dur = {"route": 0.0, "gate_up": 0.0, "down": 0.0}
+    kern_ms = 0.0
     prof_steps = max(1, min(args.steps, 20))
     with torch.cuda.stream(stream):
         for _ in range(prof_steps):
@@ -342,16 +330,13 @@ def run_ours(args, rank, world, local):
                                     stream.cuda_stream, [e.cuda_event for e in evs[l]])
             stream.synchronize()
             for l in range(n_layers):
-                e = evs[l]
-                dur["route"] += e[0].elapsed_time(e[1])
-                dur["gate_up"] += e[1].elapsed_time(e[2])
-                dur["down"] += e[2].elapsed_time(e[3])
+                kern_ms += evs[l][0].elapsed_time(evs[l][1])
     launches = prof_steps * n_layers
-    gu_bytes = sum(gate_up_bytes(shape, rows, U[l], rowcnt[l]) for l in range(n_layers))
-    gu_ms = dur["gate_up"] / launches
+    step_bytes = sum(layer_bytes(shape, rows, u) for u in U)
+    kernel_ms = kern_ms / launches
     peak, peak_kind = hbm_peak()
-    achieved = gu_bytes / n_layers / (gu_ms * 1e-3) / 1e9
-    traffic = committed_traffic("moe_gate_up_kernel", args.workload, rows)
+    achieved = step_bytes / n_layers / (kernel_ms * 1e-3) / 1e9
+    traffic = committed_traffic("moe_layer_kernel", args.workload, rows)
 
     # end to end through the public API with host buffers
     x_host = xbuf.cpu().pin_memory()
@@ -373,7 +358,6 @@ def run_ours(args, rank, world, local):
     if ws.status() != 0:
         raise RuntimeError("device status set during the timed region")
 
-    step_bytes = sum(layer_bytes(shape, rows, u) for u in U)
     layer_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
@@ -385,21 +369,21 @@ def run_ours(args, rank, world, local):
             "union_mean": round(sum(U) / len(U), 3),
             "l2": "no flush: each step streams %.2f GB of distinct weights (L2 129 MB)"
                   % (step_bytes / 1e9),
-            "graph": "one CUDA graph of %d layers x 3 PDL-chained kernels" % n_layers,
+            "graph": "one CUDA graph of %d layers, one persistent kernel each, "
+                     "PDL-chained" % n_layers,
             "parallelism": "replicas" if world > 1 else "single GPU"}),
         "weight_gbs": round(layer_gbs, 1),
         "weight_frac_of_peak": round(layer_gbs / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "moe_gate_up_kernel",
+        "roofline": {"bound": "hbm", "kernel": "moe_layer_kernel",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peak_kind,
-                     "kernel_ms": round(gu_ms, 5),
-                     "kernel_share": {k: round(v / sum(dur.values()), 4)
-                                      for k, v in dur.items()}},
+                     "algorithmic_bytes_per_launch": int(step_bytes / n_layers),
+                     "kernel_us": round(kernel_ms * 1000, 3)},
         "e2e": {"value": round(e2e_value, 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(out_host.numel() * 2)},
-        "gpu_launches": 3 * n_layers * args.steps,
+        "gpu_launches": n_layers * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

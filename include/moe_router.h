@@ -205,16 +205,15 @@ MOE_API moe_status moe_forward(const moe_config *cfg, const moe_weights *w,
                        const uint16_t *x, uint16_t *out, int rows, void *ws,
                        size_t ws_bytes, void *stream);
 
-/* moe_forward with CUDA events recorded around its three launches, for
- * per-kernel timing: ev[0] before the router/top-k/union kernel, ev[1]
- * after it, ev[2] after the gate+up kernel, ev[3] after the down+blend
- * kernel (each a cudaEvent_t passed as void*).  The event records sit
- * between the launches, so the launches do not overlap their prologues as
- * they do in moe_forward; the result bytes are the same.  Diagnostics. */
+/* moe_forward with CUDA events recorded just before and just after the
+ * layer's kernel launch (ev[0], ev[1]: cudaEvent_t passed as void*), for
+ * timing the kernel alone.  The event records sit between launches, so the
+ * kernel does not overlap its prologue with the previous launch as it does
+ * in moe_forward; the result bytes are the same.  Diagnostics. */
 MOE_API moe_status moe_forward_timed(const moe_config *cfg, const moe_weights *w,
                                      const uint16_t *x, uint16_t *out, int rows,
                                      void *ws, size_t ws_bytes, void *stream,
-                                     void *const ev[4]);
+                                     void *const ev[2]);
 
 /* Bytes of the library-owned device workspace behind moe_forward_static;
  * it covers every configuration moe_check_config accepts (at most about

@@ -1,7 +1,7 @@
 // moe_api.cu -- host side of the C ABI declared in include/moe_router.h:
-// argument checks (all before the first launch), workspace layout, and the
-// launch sequence route -> gate+up -> down+blend, chained with programmatic
-// dependent launch on the caller's stream.
+// argument checks (all before the first launch), workspace layout, the launch
+// of the persistent layer kernel (programmatic dependent launch on the
+// caller's stream) and of the stage kernels behind moe_route / moe_union.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -15,13 +15,10 @@
 namespace moe {
 cudaError_t launch_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_union(const UnionParams &p, cudaStream_t stream);
-cudaError_t launch_gate_up(const ExpertParams &p, int grid, size_t smem, int maxc,
-                           cudaStream_t stream);
-cudaError_t launch_down(const ExpertParams &p, int grid, int W, size_t smem, int maxc,
-                        cudaStream_t stream);
-cudaError_t set_expert_smem_limits(int bytes);
-size_t gate_up_fixed_smem(int stages);
-size_t down_fixed_smem(int stages);
+cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
+                         cudaStream_t stream);
+cudaError_t set_layer_smem_limit(int bytes);
+size_t layer_smem_bytes(int stages, uint32_t slot_bytes);
 }  // namespace moe
 
 using namespace moe;
@@ -67,7 +64,7 @@ moe_status device_info(DevInfo **out) {
             (e = cudaDeviceGetAttribute(&di.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                         d)) != cudaSuccess)
             return fail(MOE_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
-        if ((e = set_expert_smem_limits(di.smem_optin - 1024)) != cudaSuccess)
+        if ((e = set_layer_smem_limit(di.smem_optin - 1024)) != cudaSuccess)
             return fail(MOE_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
         di.attrs_set = true;
     }
@@ -323,77 +320,55 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     if ((s = device_info(&di)) != MOE_OK) return s;
 
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const WsPtrs wp = ws_ptrs(ws, L);
-    RouteParams rp = route_params(cfg, w, x, rows, wp);
-    rp.do_union = 1;
+    LayerParams lp{};
+    lp.H = cfg->hidden;
+    lp.E = cfg->num_experts;
+    lp.k = cfg->top_k;
+    lp.rows = rows;
+    lp.I = cfg->moe_inter;
+    lp.Is = cfg->has_shared ? cfg->shared_inter : 0;
+    lp.scoring = cfg->scoring;
+    lp.norm = cfg->norm_topk_prob;
+    lp.router_fmt = cfg->router_fmt;
+    lp.has_shared = cfg->has_shared;
+    lp.shared_gated = cfg->has_shared && cfg->shared_gate;
+    lp.per_row_mode = cfg->per_row_mode;
+    lp.rsf = cfg->routed_scaling_factor;
+    lp.x = x;
+    lp.out = out;
+    lp.router_bf16 = w->router_bf16;
+    lp.router_fp4 = w->router_nvfp4;
+    lp.bias = w->correction_bias;
+    lp.sh_vec = w->shared_expert_gate;
+    lp.gate = w->gate;
+    lp.up = w->up;
+    lp.down = w->down;
+    lp.sh_gate = w->shared_gate_proj;
+    lp.sh_up = w->shared_up_proj;
+    lp.sh_down = w->shared_down_proj;
+    lp.ws = ws_ptrs(ws, L);
+
+    // Ring slot = one 16-row gate or up tile (16 x H/2 packed + 16 x H/16
+    // scale bytes) or one 32-row down tile (32 x I/2 + 32 x I/16); a gate+up
+    // unit takes two slots, a down unit one.
+    const size_t gu_slot = (size_t)kTileRows * (cfg->hidden / 2 + cfg->hidden / 16);
+    const size_t d_slot = (size_t)kOutTile * (L.inter_max / 2 + L.inter_max / 16);
+    lp.slot_bytes = (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot);
+    const int budget = di->smem_optin - 1024;
+    int S = 16;
+    while (S > 2 && layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget) --S;
+    if (layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget)
+        return fail(MOE_ERR_UNSUPPORTED, "stage ring does not fit in shared memory");
+    lp.stages = S;
+    const int mc_gu = (cfg->hidden / kChunk + kConsumerWarps - 1) / kConsumerWarps;
+    const int mc_d = (L.inter_max / kChunk + kConsumerWarps - 1) / kConsumerWarps;
+
     cudaError_t e = cudaSuccess;
-    auto mark = [&](int i) {
-        if (ev && e == cudaSuccess) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
-    };
-    mark(0);
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "event record: %s", cudaGetErrorString(e));
-    e = launch_route(rp, st);
-    mark(1);
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
-
-    ExpertParams ep{};
-    ep.H = cfg->hidden;
-    ep.I = cfg->moe_inter;
-    ep.Is = cfg->has_shared ? cfg->shared_inter : 0;
-    ep.k = cfg->top_k;
-    ep.rows = rows;
-    ep.has_shared = cfg->has_shared;
-    ep.x = x;
-    ep.out = out;
-    ep.sh_gate = w->shared_gate_proj;
-    ep.sh_up = w->shared_up_proj;
-    ep.sh_down = w->shared_down_proj;
-    ep.ws = wp;
-    const int smem_budget = di->smem_optin - 1024;
-    const int max_entries = (rows * cfg->top_k < cfg->num_experts ? rows * cfg->top_k
-                                                                   : cfg->num_experts);
-
-    // gate + up: stage = gate and up tiles (16 rows x H/2 packed + H/16 scales each)
-    {
-        const int nchunk = cfg->hidden / kChunk;
-        const int maxc = (nchunk + kConsumerWarps - 1) / kConsumerWarps;
-        ep.stage_bytes = (uint32_t)(2 * kTileRows * (cfg->hidden / 2 + cfg->hidden / 16));
-        int S = 8;
-        while (S > 2 && S * (size_t)ep.stage_bytes + gate_up_fixed_smem(S) > (size_t)smem_budget)
-            --S;
-        ep.stages = S;
-        const size_t smem = S * (size_t)ep.stage_bytes + gate_up_fixed_smem(S);
-        if (smem > (size_t)smem_budget)
-            return fail(MOE_ERR_UNSUPPORTED, "gate+up stage ring needs %zu bytes of shared memory",
-                        smem);
-        const int units = (cfg->has_shared ? ep.Is / kTileRows : 0) +
-                          max_entries * (cfg->moe_inter / kTileRows);
-        const int grid = units < di->sms ? units : di->sms;
-        e = launch_gate_up(ep, grid, smem, maxc, st);
-        mark(2);
-        if (e != cudaSuccess)
-            return fail(MOE_ERR_CUDA, "gate+up launch: %s", cudaGetErrorString(e));
-    }
-    // down + weighted sum + blend: stage = one 16-row tile of Wd
-    {
-        const int kmax = L.inter_max;
-        const int nchunk = kmax / kChunk;
-        const int maxc = (nchunk + kConsumerWarps - 1) / kConsumerWarps;
-        const int W = (nchunk + maxc - 1) / maxc;
-        ep.stage_bytes = (uint32_t)(kTileRows * (kmax / 2 + kmax / 16));
-        int S = 16;
-        while (S > 2 && S * (size_t)ep.stage_bytes + down_fixed_smem(S) > (size_t)smem_budget)
-            --S;
-        ep.stages = S;
-        const size_t smem = S * (size_t)ep.stage_bytes + down_fixed_smem(S);
-        const int units = (cfg->has_shared ? cfg->hidden / kTileRows : 0) +
-                          max_entries * (cfg->hidden / kTileRows);
-        const int grid = units < di->sms ? units : di->sms;
-        e = launch_down(ep, grid, W, smem, maxc, st);
-        mark(3);
-        if (e != cudaSuccess)
-            return fail(MOE_ERR_CUDA, "down launch: %s", cudaGetErrorString(e));
-    }
+    if (ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st);
+    if (e == cudaSuccess)
+        e = launch_layer(lp, di->sms, layer_smem_bytes(S, lp.slot_bytes), mc_gu, mc_d, st);
+    if (e == cudaSuccess && ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), st);
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "layer launch: %s", cudaGetErrorString(e));
     return ok();
 }
 
@@ -406,9 +381,8 @@ moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16
 
 moe_status moe_forward_timed(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
                              uint16_t *out, int rows, void *ws, size_t ws_bytes, void *stream,
-                             void *const ev[4]) {
-    if (!ev || !ev[0] || !ev[1] || !ev[2] || !ev[3])
-        return fail(MOE_ERR_INVALID_ARG, "four events are required");
+                             void *const ev[2]) {
+    if (!ev || !ev[0] || !ev[1]) return fail(MOE_ERR_INVALID_ARG, "two events are required");
     return forward_impl(cfg, w, x, out, rows, ws, ws_bytes, stream, ev);
 }
 

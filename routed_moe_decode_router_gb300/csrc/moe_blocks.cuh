@@ -1,0 +1,535 @@
+// moe_blocks.cuh -- device building blocks shared by the route kernel and the
+// layer kernel: warp top-k, pairwise-scan union, pointer entries, the NVFP4
+// x f16 MMA on one 128-input chunk, token-row fragments, the stage-ring wait
+// and the grid barrier.
+#pragma once
+
+#include "moe_device.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Pointer entries
+// ---------------------------------------------------------------------------
+
+// Pointer entry (gate, up, down matrices) of expert x from the expert tables.
+__device__ __forceinline__ void load_ptr_entry(const moe_expert_table *tabs, int x, PtrEntry &e) {
+#pragma unroll
+    for (int m = 0; m < 3; ++m) {
+        e.packed[m] = ld_cg(tabs[m].packed + x);
+        e.scales[m] = ld_cg(tabs[m].scales + x);
+        e.scale2[m] = ld_cg(tabs[m].scale2 + x);
+    }
+    e.expert = x;
+}
+
+__device__ __forceinline__ bool aligned16(const void *p) {
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+// ---------------------------------------------------------------------------
+// Top-k of one token row (one warp)
+// ---------------------------------------------------------------------------
+//
+// Selection key (forward_token_major.rs: moe_topk_softmax_batched /
+// moe_topk_sigmoid_batched): the logit for softmax scoring (softmax is
+// strictly increasing in it), sigmoid(logit) + correction bias for sigmoid
+// scoring; largest key first, equal keys to the lower expert id, NaN keys
+// rank lowest.  Weights: softmax -> exp(l_j - l_max) over the selected slots
+// (norm_topk_prob) or over all experts; sigmoid -> sigmoid(l_j), normalised
+// over the selected slots when norm_topk_prob, times routed_scaling_factor.
+// All arithmetic is fp32 (expf, IEEE division); the sums are compensated.
+
+// Orderable 64-bit form of (key, id): larger key first, then lower id.
+// Any real key packs above 0, the value of an empty candidate.
+__device__ __forceinline__ unsigned long long pack_key_id(float key, int id) {
+    uint32_t u = __float_as_uint(key);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // monotone float -> uint
+    return ((unsigned long long)u << 32) | (uint32_t)(0x7fffffff - id);
+}
+
+// Error-free sum a + b = s + e (Knuth's TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = a + b;
+    const float bb = s - a;
+    e = (a - (s - bb)) + (b - bb);
+}
+
+// Compensated warp sum: every lane gets the same result, within about one
+// rounding of the exact sum of the 32 lanes' (value, error) pairs.
+__device__ __forceinline__ float warp_sum_compensated(float v, float c) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const float c2 = __shfl_xor_sync(0xffffffffu, c, o);
+        float s, e;
+        two_sum(v, v2, s, e);
+        v = s;
+        c = (c + c2) + e;
+    }
+    return v + c;
+}
+
+// Descending bitonic sort of NK packed candidates (values carried along).
+template <int NK>
+__device__ __forceinline__ void sort_desc(unsigned long long (&c)[NK], float (&v)[NK]) {
+#pragma unroll
+    for (int size = 2; size <= NK; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+            for (int i = 0; i < NK; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const bool desc = (i & size) == 0;
+                    const bool sw = desc ? (c[i] < c[j]) : (c[i] > c[j]);
+                    const unsigned long long ci = c[i], cj = c[j];
+                    const float vi = v[i], vj = v[j];
+                    c[i] = sw ? cj : ci;
+                    c[j] = sw ? ci : cj;
+                    v[i] = sw ? vj : vi;
+                    v[j] = sw ? vi : vj;
+                }
+            }
+        }
+    }
+}
+
+// Each lane holds NL sorted lists of NK candidates (experts
+// lane + 32 * (list * NK + i)), so E <= 32 * NK * NL; the keys are loaded
+// once.  Every selection is two warp max reductions (key, then the lowest id
+// among equal keys) over the lanes' best heads and a shift of the winner's
+// list.
+template <int NK, int NL>
+__device__ __forceinline__ void warp_topk_row_nk(const float *lg, const float *bias, int E, int k,
+                                                 int scoring, int norm, float rsf,
+                                                 int32_t *ids_out, float *wts_out, int lane) {
+    const unsigned FULL = 0xffffffffu;
+    const bool sigm = scoring == MOE_SCORING_SIGMOID;
+    unsigned long long c[NL][NK];
+    float v[NL][NK];
+#pragma unroll
+    for (int L = 0; L < NL; ++L) {
+#pragma unroll
+        for (int i = 0; i < NK; ++i) {
+            const int e = lane + 32 * (L * NK + i);
+            c[L][i] = 0ull;
+            v[L][i] = 0.f;
+            if (e < E) {
+                const float l = ld_cg(lg + e);
+                float kv;
+                if (sigm) {
+                    v[L][i] = 1.f / (1.f + expf(-l));
+                    kv = v[L][i] + bias[e];
+                } else {
+                    v[L][i] = l;
+                    kv = l;
+                }
+                if (kv != kv) kv = -INFINITY;   // NaN ranks lowest
+                kv += 0.f;                       // -0 ranks as +0
+                c[L][i] = pack_key_id(kv, e);
+            }
+        }
+        sort_desc<NK>(c[L], v[L]);
+    }
+    int my_id0 = 0, my_id1 = 0;     // expert of slots lane and lane + 32
+    float my_v0 = 0.f, my_v1 = 0.f; // its logit (softmax) or sigmoid (sigmoid scoring)
+    for (int j = 0; j < k; ++j) {
+        int from = 0;
+        unsigned long long head = c[0][0];
+        float hv = v[0][0];
+#pragma unroll
+        for (int L = 1; L < NL; ++L) {
+            if (c[L][0] > head) {
+                head = c[L][0];
+                hv = v[L][0];
+                from = L;
+            }
+        }
+        const uint32_t hi = (uint32_t)(head >> 32), lo = (uint32_t)head;
+        const uint32_t mk = __reduce_max_sync(FULL, hi);
+        const uint32_t ml = __reduce_max_sync(FULL, hi == mk ? lo : 0u);
+        const int bi = 0x7fffffff - (int)ml;
+        const float bv = __shfl_sync(FULL, hv, bi & 31);
+        if (hi == mk && lo == ml) {   // the winner lane drops the head of its list
+#pragma unroll
+            for (int L = 0; L < NL; ++L) {
+                if (L == from) {
+#pragma unroll
+                    for (int i = 0; i + 1 < NK; ++i) {
+                        c[L][i] = c[L][i + 1];
+                        v[L][i] = v[L][i + 1];
+                    }
+                    c[L][NK - 1] = 0ull;
+                }
+            }
+        }
+        if (lane == (j & 31)) {
+            if (j < 32) {
+                my_id0 = bi;
+                my_v0 = bv;
+            } else {
+                my_id1 = bi;
+                my_v1 = bv;
+            }
+        }
+    }
+    // routing weights: lane j (and j + 32) owns slot j
+    const float top = __shfl_sync(FULL, my_v0, 0);   // slot 0 holds the largest logit
+    float w[2] = {0.f, 0.f};
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+        if (lane + 32 * h < k) w[h] = sigm ? (h ? my_v1 : my_v0) : expf((h ? my_v1 : my_v0) - top);
+    float denom = 1.f;
+    if (norm) {
+        float s, e;
+        two_sum(w[0], w[1], s, e);
+        denom = warp_sum_compensated(s, e);
+    } else if (!sigm) {
+        // softmax without renormalisation: the full denominator over all E
+        float zsum = 0.f, zerr = 0.f;
+        for (int e = lane; e < E; e += 32) {
+            float s, er;
+            two_sum(zsum, expf(ld_cg(lg + e) - top), s, er);
+            zsum = s;
+            zerr += er;
+        }
+        denom = warp_sum_compensated(zsum, zerr);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = lane + 32 * h;
+        if (j < k) {
+            ids_out[j] = h ? my_id1 : my_id0;
+            float wj = w[h] / denom;
+            if (sigm) wj *= rsf;
+            wts_out[j] = wj;
+        }
+    }
+}
+
+__device__ __forceinline__ void warp_topk_row(const float *lg, const float *bias, int E, int k,
+                                              int scoring, int norm, float rsf, int32_t *ids_out,
+                                              float *wts_out, int lane) {
+    if (E <= 128)
+        warp_topk_row_nk<4, 1>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+    else if (E <= 256)
+        warp_topk_row_nk<8, 1>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+    else if (E <= 512)
+        warp_topk_row_nk<16, 1>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+    else
+        warp_topk_row_nk<16, 2>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Union + pointer table (one warp)
+// ---------------------------------------------------------------------------
+
+struct UnionSrc {
+    int E, k, rows, per_row_mode, has_tables, has_shared;
+    moe_expert_table gate, up, down;
+    moe_nvfp4 sh_gate, sh_up, sh_down;
+};
+
+// Union of the rows * k ids in s_ids (position p = row * k + slot) by
+// pairwise scan (page "Function forward_moe", RETRACTED note): position p
+// opens a union entry when no earlier position holds the same id; entries
+// keep first-occurrence order; no sort.  Lane l holds positions l and l + 32;
+// the comparisons against earlier positions run on registers (warp match
+// within a half, shuffles across the halves).  Writes the table and, with
+// has_tables, the pointer entry of every union expert plus the shared expert
+// at kSharedEntry.  `ut` and `ptrs` may point to shared or global memory;
+// s_mask is 64 words of scratch shared memory.  All 32 lanes of one warp
+// call it.
+__device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, uint32_t *s_mask,
+                                   moe_union_table *ut, PtrEntry *ptrs, WsHeader *hdr, int lane) {
+    const unsigned FULL = 0xffffffffu;
+    const int n = src.rows * src.k;
+    const int p0 = lane, p1 = lane + 32;
+    // unused positions get distinct negative ids, so they never match
+    const int id0 = p0 < n ? s_ids[p0] : -1 - p0;
+    const int id1 = p1 < n ? s_ids[p1] : -1 - p1;
+    const unsigned below = (1u << lane) - 1u;
+    unsigned eq0, eq1, cross = 0;   // same-id lanes: half 0 for id0, half 1 for id1, half 0 for id1
+    if (src.per_row_mode) {
+        eq0 = 1u << lane;
+        eq1 = 1u << lane;
+    } else {
+        eq0 = __match_any_sync(FULL, id0);
+        eq1 = __match_any_sync(FULL, id1);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) cross |= (__shfl_sync(FULL, id0, q) == id1 ? 1u : 0u) << q;
+    }
+    const bool first0 = p0 < n && (eq0 & below) == 0;
+    const bool first1 = p1 < n && cross == 0 && (eq1 & below) == 0;
+    const unsigned f0 = __ballot_sync(FULL, first0);
+    const unsigned f1 = __ballot_sync(FULL, first1);
+    const int U = __popc(f0) + __popc(f1);
+    const int uidx0 = __popc(f0 & below);
+    const int uidx1 = __popc(f0) + __popc(f1 & below);
+    // union index of every position: that of its first occurrence (every
+    // lane runs every shuffle: a full-mask shuffle must not diverge)
+    const int u0 = __shfl_sync(FULL, uidx0, __ffs(eq0) - 1);
+    const int u1_cross = __shfl_sync(FULL, uidx0, cross ? __ffs(cross) - 1 : lane);
+    const int u1_half = __shfl_sync(FULL, uidx1, __ffs(eq1) - 1);
+    const int u1 = cross ? u1_cross : u1_half;
+    s_mask[lane] = 0u;
+    s_mask[lane + 32] = 0u;
+    for (int i = lane; i < kMaxIds * kMaxRows; i += 32) (&ut->uslot[0][0])[i] = 0xFF;
+    __syncwarp();
+    const int k = src.k;
+    if (p0 < n) {
+        ut->slot2u[p0] = (uint8_t)u0;
+        ut->uslot[u0][p0 / k] = (uint8_t)(p0 % k);
+        atomicOr(&s_mask[u0], 1u << (p0 / k));
+    }
+    if (p1 < n) {
+        ut->slot2u[p1] = (uint8_t)u1;
+        ut->uslot[u1][p1 / k] = (uint8_t)(p1 % k);
+        atomicOr(&s_mask[u1], 1u << (p1 / k));
+    }
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const bool first = h ? first1 : first0;
+        if (!first) continue;
+        const int p = h ? p1 : p0;
+        const int u = h ? uidx1 : uidx0;
+        const int x = h ? id1 : id0;
+        ut->expert[u] = x;
+        ut->rowmask[u] = (uint8_t)s_mask[u];
+        if (src.has_tables) {
+            PtrEntry e;
+            if (x < 0 || x >= src.E) {
+                record_fault(hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)p);
+                e = PtrEntry{};
+                e.expert = -1;
+            } else {
+                const moe_expert_table tb[3] = {src.gate, src.up, src.down};
+                load_ptr_entry(tb, x, e);
+                bool ok = true;
+#pragma unroll
+                for (int m = 0; m < 3; ++m)
+                    ok = ok && aligned16(e.packed[m]) && aligned16(e.scales[m]);
+                if (!ok) {
+                    record_fault(hdr, MOE_DEV_MISALIGNED_PTR, (uint32_t)x);
+                    e.expert = -1;
+                }
+            }
+            ptrs[u] = e;
+        } else if (x < 0 || x >= src.E) {
+            record_fault(hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)p);
+        }
+    }
+    if (lane == 0) {
+        if (src.has_tables && src.has_shared) {
+            PtrEntry e;
+            const moe_nvfp4 *sm[3] = {&src.sh_gate, &src.sh_up, &src.sh_down};
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                e.packed[m] = sm[m]->packed;
+                e.scales[m] = sm[m]->scales;
+                e.scale2[m] = sm[m]->scale2;
+            }
+            e.expert = kSharedEntry;
+            ptrs[kSharedEntry] = e;
+        }
+        ut->rows = src.rows;
+        ut->top_k = src.k;
+        ut->per_row_mode = src.per_row_mode;
+        ut->num_union = U;
+    }
+}
+
+// Pointer entries of the union experts (entries u < U of `ut`), one lane per
+// entry, with the range and alignment checks of build_union; used when the
+// union was built without tables.  All 32 lanes of one warp call it.
+__device__ inline void load_union_ptrs(const moe_union_table *ut, int U, int E,
+                                       const moe_expert_table *tabs, PtrEntry *ptrs, WsHeader *hdr,
+                                       int lane) {
+    for (int u = lane; u < U; u += 32) {
+        const int x = ut->expert[u];
+        PtrEntry e;
+        if (x < 0 || x >= E) {
+            record_fault(hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)u);
+            e = PtrEntry{};
+            e.expert = -1;
+        } else {
+            load_ptr_entry(tabs, x, e);
+            bool ok = true;
+#pragma unroll
+            for (int m = 0; m < 3; ++m) ok = ok && aligned16(e.packed[m]) && aligned16(e.scales[m]);
+            if (!ok) {
+                record_fault(hdr, MOE_DEV_MISALIGNED_PTR, (uint32_t)x);
+                e.expert = -1;
+            }
+        }
+        ptrs[u] = e;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 x f16 MMA on one 128-input chunk of a 16-row tile
+// ---------------------------------------------------------------------------
+//
+// Lane (g = lane/4, q = lane%4) reads 16 bytes (32 inputs) of rows g and g+8
+// at input offset q*32 inside the chunk, plus their two E4M3 scales; MMA
+// step s (0..7) uses inputs 4s..4s+3 of that slice: logical k (2q, 2q+1) <-
+// inputs (4s, 4s+1) and (2q+8, 2q+9) <- (4s+2, 4s+3).  The B fragments hold
+// the token rows at the same inputs.  E2M1 x E4M3 is exact in f16.  Even
+// steps accumulate into d0, odd steps into d1 (two independent MMA chains);
+// the caller adds d0 + d1 in that order.
+__device__ __forceinline__ void chunk_mma(const uint8_t *pk, const uint8_t *sc, int row_bytes,
+                                          int sc_row_bytes, int c, int g, int q,
+                                          const uint32_t (&b)[8][2], float (&d0)[4],
+                                          float (&d1)[4]) {
+    const uint4 wa = *reinterpret_cast<const uint4 *>(pk + g * row_bytes + c * 64 + q * 16);
+    const uint4 wb =
+        *reinterpret_cast<const uint4 *>(pk + (g + 8) * row_bytes + c * 64 + q * 16);
+    const uint32_t sa = *reinterpret_cast<const uint16_t *>(sc + g * sc_row_bytes + c * 8 + q * 2);
+    const uint32_t sb =
+        *reinterpret_cast<const uint16_t *>(sc + (g + 8) * sc_row_bytes + c * 8 + q * 2);
+    const uint32_t fa = e4m3x2_to_f16x2(sa), fb = e4m3x2_to_f16x2(sb);
+    const uint32_t sa0 = bcast_lo(fa), sa1 = bcast_hi(fa);
+    const uint32_t sb0 = bcast_lo(fb), sb1 = bcast_hi(fb);
+    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        uint32_t ha[4], hb[4];
+        e2m1x8_to_f16x2(wA[t], ha);
+        e2m1x8_to_f16x2(wB[t], hb);
+        const uint32_t scA = t < 2 ? sa0 : sa1;
+        const uint32_t scB = t < 2 ? sb0 : sb1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ha[i] = hmul2(ha[i], scA);
+            hb[i] = hmul2(hb[i], scB);
+        }
+        mma_f16_16816(d0, ha[0], hb[0], ha[1], hb[1], b[2 * t][0], b[2 * t][1]);
+        mma_f16_16816(d1, ha[2], hb[2], ha[3], hb[3], b[2 * t + 1][0], b[2 * t + 1][1]);
+    }
+}
+
+// B fragments of one token-row matrix (x or h) for this warp's chunks
+// (chunk c = warp + nwarps*m): lane (n = lane/4, q = lane%4) takes row n's 32
+// inputs at c*128 + q*32, in one pass of L2 loads; rows outside `mask` are
+// zero.  The bf16 values are scaled by 2^e (e per row, from the largest
+// magnitude over this warp's chunks) and converted to f16 in place.  inv0 /
+// inv1 receive 2^-e of the D columns 2q and 2q+1.
+template <int MAXC>
+__device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_stride,
+                                       uint32_t mask, int nchunk, int warp, int nwarps,
+                                       int lane, uint32_t (&b)[MAXC][8][2], float &inv0,
+                                       float &inv1) {
+    const int n = lane >> 2, q = lane & 3;
+    const bool on = (mask >> n) & 1u;
+#pragma unroll
+    for (int m = 0; m < MAXC; ++m) {
+        const int c = warp + nwarps * m;
+        const bool live = on && c < nchunk;
+        const uint16_t *src = rows_base + (size_t)n * row_stride + c * kChunk + q * 32;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            uint4 xv = make_uint4(0u, 0u, 0u, 0u);
+            if (live) xv = ld_cg_v4(src + 8 * v);
+            b[m][2 * v][0] = xv.x;
+            b[m][2 * v][1] = xv.y;
+            b[m][2 * v + 1][0] = xv.z;
+            b[m][2 * v + 1][1] = xv.w;
+        }
+    }
+    float mx = 0.f;
+#pragma unroll
+    for (int m = 0; m < MAXC; ++m)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(b[m][s][h])), fabsf(bf16_hi(b[m][s][h]))));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const int e = f16_block_exponent(mx);
+    const float up = exp2i(e);
+#pragma unroll
+    for (int m = 0; m < MAXC; ++m)
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                b[m][s][h] = pack_f16x2(bf16_lo(b[m][s][h]) * up, bf16_hi(b[m][s][h]) * up);
+    const float inv = exp2i(-e);
+    inv0 = __shfl_sync(0xffffffffu, inv, 8 * q);
+    inv1 = __shfl_sync(0xffffffffu, inv, 8 * q + 4);
+}
+
+// D fragment (lane g, q: rows g / g+8, columns 2q / 2q+1) -> smem, column
+// major [8 columns][16 rows], so that a column's 16 rows are contiguous.
+__device__ __forceinline__ void store_partial(float *dst, const float (&d)[4], int g, int q,
+                                              float inv0, float inv1) {
+    dst[(2 * q) * 16 + g] = d[0] * inv0;
+    dst[(2 * q + 1) * 16 + g] = d[1] * inv1;
+    dst[(2 * q) * 16 + g + 8] = d[2] * inv0;
+    dst[(2 * q + 1) * 16 + g + 8] = d[3] * inv1;
+}
+
+// ---------------------------------------------------------------------------
+// Stage ring wait and grid barrier, both bounded
+// ---------------------------------------------------------------------------
+
+// Wait for the phase of `bar` with the given parity.  Gives up at once when
+// the CTA's abort flag is set; after kWaitLimitCycles it records
+// MOE_DEV_WAIT_TIMEOUT, sets the abort flag and gives up.
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          WsHeader *hdr, uint32_t info) {
+    if (*abort) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            record_fault(hdr, MOE_DEV_WAIT_TIMEOUT, info);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// One arrival of this CTA at the grid barrier (called by one thread, after
+// the CTA's own barrier, which orders the CTA's earlier writes before the
+// release).  The counter only grows: arrival n belongs to episode n / G, and
+// the episode ends when the counter reaches (episode + 1) * G, so there is
+// no reset and no second atomic.  The spin is bounded: on timeout it records
+// MOE_DEV_WAIT_TIMEOUT, sets the abort flag and returns false.  Requires
+// every CTA of the grid to be resident at once (cooperative launch).
+__device__ __forceinline__ bool grid_arrive_wait(unsigned long long *count, unsigned nblocks,
+                                                 volatile int *abort, WsHeader *hdr,
+                                                 uint32_t info) {
+    unsigned long long old;
+    asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;"
+                 : "=l"(old)
+                 : "l"(count)
+                 : "memory");
+    const unsigned long long target = (old / nblocks + 1) * nblocks;
+    if (ld_acquire_u64(count) >= target) return true;
+    const long long t0 = clock64();
+    while (ld_acquire_u64(count) < target) {
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            record_fault(hdr, MOE_DEV_WAIT_TIMEOUT, info);
+            return false;
+        }
+        __nanosleep(20);
+    }
+    return true;
+}
+
+}  // namespace moe

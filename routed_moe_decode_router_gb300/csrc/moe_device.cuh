@@ -100,33 +100,19 @@ __device__ __forceinline__ void named_bar(int id, int count) {
 // ---------------------------------------------------------------------------
 // Loads that bypass L1 (data written by other CTAs or earlier kernels)
 // ---------------------------------------------------------------------------
+// L2-only loads of data written by other CTAs or by earlier kernels.
+__device__ __forceinline__ float ld_cg(const float *p) { return __ldcg(p); }
+__device__ __forceinline__ int ld_cg(const int *p) { return __ldcg(p); }
+__device__ __forceinline__ unsigned ld_cg(const unsigned *p) { return __ldcg(p); }
+__device__ __forceinline__ uint8_t ld_cg(const uint8_t *p) {
+    return (uint8_t)__ldcg(reinterpret_cast<const unsigned char *>(p));
+}
 template <typename T>
-__device__ __forceinline__ T ld_cg(const T *p) {
-    static_assert(sizeof(T) == 1 || sizeof(T) == 4 || sizeof(T) == 8, "ld_cg size");
-    T r;
-    if constexpr (sizeof(T) == 8) {
-        unsigned long long v;
-        asm volatile("ld.global.cg.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-        __builtin_memcpy(&r, &v, 8);
-    } else if constexpr (sizeof(T) == 4) {
-        unsigned v;
-        asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-        __builtin_memcpy(&r, &v, 4);
-    } else {
-        unsigned short v;
-        asm volatile("ld.global.cg.u8 %0, [%1];" : "=h"(v) : "l"(p) : "memory");
-        const unsigned char c = (unsigned char)v;
-        __builtin_memcpy(&r, &c, 1);
-    }
-    return r;
+__device__ __forceinline__ T *ld_cg(T *const *p) {
+    return reinterpret_cast<T *>(__ldcg(reinterpret_cast<const unsigned long long *>(p)));
 }
 __device__ __forceinline__ uint4 ld_cg_v4(const void *p) {
-    uint4 v;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p)
-                 : "memory");
-    return v;
+    return __ldcg(reinterpret_cast<const uint4 *>(p));
 }
 __device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
     uint4 v;

@@ -13,9 +13,10 @@ constexpr int kMaxRows = MOE_MAX_ROWS;
 constexpr int kMaxIds = MOE_MAX_IDS;
 constexpr int kSharedEntry = kMaxIds;    // pointer-table slot of the shared expert
 constexpr int kEntries = kMaxIds + 1;
-constexpr int kTileRows = 16;            // output rows per work unit (MMA M)
-constexpr int kChunk = 128;              // inputs per consumer-warp chunk
-constexpr int kConsumerWarps = 8;        // gate+up kernel
+constexpr int kTileRows = 16;            // output rows of one MMA tile (M)
+constexpr int kOutTile = 32;             // output rows of a down unit / blend tile
+constexpr int kChunk = 128;              // inputs per compute-warp chunk
+constexpr int kConsumerWarps = 8;        // compute warps of the layer kernel
 constexpr int kRouteWarps = 8;
 
 // Status word and counters at the start of the workspace (256 bytes).
@@ -23,7 +24,9 @@ struct WsHeader {
     uint32_t status;        // first MOE_DEV_* fault recorded (0 = none)
     uint32_t status_info;   // detail of that fault (offending id / unit)
     uint32_t route_ticket;  // last-block ticket of the route kernel
-    uint32_t pad[61];
+    uint32_t pad0;
+    unsigned long long bar_count;  // grid barrier of the layer kernel (monotonic)
+    uint32_t pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -42,15 +45,13 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // Byte offsets of every workspace region for one configuration.  The layout
 // is sized for MOE_MAX_ROWS rows, so one workspace serves every row count.
 struct WsLayout {
-    size_t header, tile_cnt, ids, wts, logits, gate_val, uni, ptrs, hbuf,
-        ybuf, ysbuf, total;
+    size_t header, ids, wts, logits, gate_val, uni, ptrs, hbuf, ybuf, ysbuf, total;
     int inter_max;          // max(I, Is): row stride of the h buffer
 
     static WsLayout make(const moe_config &c) {
         WsLayout L{};
         size_t o = 0;
         L.header = o;   o = align256(o + sizeof(WsHeader));
-        L.tile_cnt = o; o = align256(o + sizeof(uint32_t) * (size_t)(c.hidden / kTileRows));
         // forward_token_major.rs scratch order: ids, then routing weights.
         L.ids = o;      o += sizeof(int32_t) * (size_t)kMaxIds;
         L.wts = o;      o = align256(o + sizeof(float) * (size_t)kMaxIds);
@@ -71,7 +72,6 @@ struct WsLayout {
 // Pointers into one workspace.
 struct WsPtrs {
     WsHeader *hdr;
-    uint32_t *tile_cnt;
     int32_t *ids;
     float *wts;
     float *logits;
@@ -88,7 +88,6 @@ inline WsPtrs ws_ptrs(void *ws, const WsLayout &L) {
     char *b = static_cast<char *>(ws);
     WsPtrs p;
     p.hdr = reinterpret_cast<WsHeader *>(b + L.header);
-    p.tile_cnt = reinterpret_cast<uint32_t *>(b + L.tile_cnt);
     p.ids = reinterpret_cast<int32_t *>(b + L.ids);
     p.wts = reinterpret_cast<float *>(b + L.wts);
     p.logits = reinterpret_cast<float *>(b + L.logits);
@@ -131,13 +130,21 @@ struct UnionParams {
     moe_union_table *out;
 };
 
-// Parameters of the expert kernels (gate+up and down+blend).
-struct ExpertParams {
-    int H, I, Is, k, rows, has_shared, stages;
-    uint32_t stage_bytes;
+// Parameters of the persistent layer kernel.
+struct LayerParams {
+    int H, E, k, rows, I, Is;
+    int scoring, norm, router_fmt, has_shared, shared_gated, per_row_mode;
+    float rsf;
+    int stages;
+    uint32_t slot_bytes;
     const uint16_t *x;
     uint16_t *out;
-    moe_nvfp4 sh_gate, sh_up, sh_down;   // host-known shared-expert matrices
+    const uint16_t *router_bf16;
+    moe_nvfp4 router_fp4;
+    const float *bias;
+    const uint16_t *sh_vec;
+    moe_expert_table gate, up, down;
+    moe_nvfp4 sh_gate, sh_up, sh_down;
     WsPtrs ws;
 };
 

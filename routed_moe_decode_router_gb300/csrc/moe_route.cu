@@ -21,7 +21,7 @@
 // path), which the expert kernels read.
 #include <cuda_runtime.h>
 
-#include "moe_device.cuh"
+#include "moe_blocks.cuh"
 
 namespace moe {
 
@@ -111,133 +111,6 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-// ---------------------------------------------------------------------------
-// Union + pointer table (one warp)
-// ---------------------------------------------------------------------------
-
-struct UnionSrc {
-    int E, k, rows, per_row_mode, has_tables, has_shared;
-    moe_expert_table gate, up, down;
-    moe_nvfp4 sh_gate, sh_up, sh_down;
-};
-
-__device__ __forceinline__ bool aligned16(const void *p) {
-    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
-}
-
-// s_ids: the rows * k ids in shared memory (position p = row * k + slot).
-// Called by all 32 lanes of one warp.
-__device__ void build_union(const UnionSrc &src, const int32_t *s_ids, uint8_t *s_uidx,
-                            moe_union_table *ut, PtrEntry *ptrs, WsHeader *hdr, int lane) {
-    const int n = src.rows * src.k;
-    bool first[2];
-    int id[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int p = lane + 32 * h;
-        id[h] = p < n ? s_ids[p] : -1;
-        bool f = p < n;
-        if (f && !src.per_row_mode) {
-            for (int q = 0; q < p; ++q) {
-                if (s_ids[q] == id[h]) {
-                    f = false;
-                    break;
-                }
-            }
-        }
-        first[h] = f;
-    }
-    const unsigned lo = __ballot_sync(0xffffffffu, first[0]);
-    const unsigned hi = __ballot_sync(0xffffffffu, first[1]);
-    const unsigned below = (1u << lane) - 1u;
-    const int U = __popc(lo) + __popc(hi);
-    int uidx[2];
-    uidx[0] = __popc(lo & below);
-    uidx[1] = __popc(lo) + __popc(hi & below);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-        if (first[h]) s_uidx[lane + 32 * h] = (uint8_t)uidx[h];
-    // clear the per-row slot table of every union entry
-    for (int i = lane; i < kMaxIds * kMaxRows; i += 32) (&ut->uslot[0][0])[i] = 0xFF;
-    __syncwarp();
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int p = lane + 32 * h;
-        if (p >= n) continue;
-        int u;
-        if (first[h]) {
-            u = uidx[h];
-        } else {
-            int q = 0;
-            while (s_ids[q] != id[h]) ++q;   // the first occurrence exists
-            u = s_uidx[q];
-        }
-        ut->slot2u[p] = (uint8_t)u;
-        ut->uslot[u][p / src.k] = (uint8_t)(p % src.k);
-        if (!first[h]) continue;
-        uint32_t mask = 0;
-        if (src.per_row_mode) {
-            mask = 1u << (p / src.k);
-        } else {
-            for (int q = 0; q < n; ++q)
-                if (s_ids[q] == id[h]) mask |= 1u << (q / src.k);
-        }
-        ut->expert[u] = id[h];
-        ut->rowmask[u] = (uint8_t)mask;
-        if (src.has_tables) {
-            PtrEntry e;
-            const int x = id[h];
-            if (x < 0 || x >= src.E) {
-                record_fault(hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)p);
-                e = PtrEntry{};
-                e.expert = -1;
-            } else {
-                const moe_expert_table *tb[3] = {&src.gate, &src.up, &src.down};
-                bool ok = true;
-#pragma unroll
-                for (int m = 0; m < 3; ++m) {
-                    e.packed[m] = tb[m]->packed[x];
-                    e.scales[m] = tb[m]->scales[x];
-                    e.scale2[m] = tb[m]->scale2[x];
-                    ok = ok && aligned16(e.packed[m]) && aligned16(e.scales[m]);
-                }
-                e.expert = x;
-                if (!ok) {
-                    record_fault(hdr, MOE_DEV_MISALIGNED_PTR, (uint32_t)x);
-                    e.expert = -1;
-                }
-            }
-            ptrs[u] = e;
-        } else if (id[h] < 0 || id[h] >= src.E) {
-            record_fault(hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)p);
-        }
-    }
-    if (lane == 0) {
-        if (src.has_tables && src.has_shared) {
-            PtrEntry e;
-            const moe_nvfp4 *sm[3] = {&src.sh_gate, &src.sh_up, &src.sh_down};
-#pragma unroll
-            for (int m = 0; m < 3; ++m) {
-                e.packed[m] = sm[m]->packed;
-                e.scales[m] = sm[m]->scales;
-                e.scale2[m] = sm[m]->scale2;
-            }
-            e.expert = kSharedEntry;
-            ptrs[kSharedEntry] = e;
-        }
-        ut->rows = src.rows;
-        ut->top_k = src.k;
-        ut->per_row_mode = src.per_row_mode;
-        ut->num_union = U;
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Route kernel
 // ---------------------------------------------------------------------------
@@ -245,8 +118,8 @@ __device__ void build_union(const UnionSrc &src, const int32_t *s_ids, uint8_t *
 __global__ void __launch_bounds__(kRouteWarps * 32)
     moe_route_kernel(const RouteParams p) {
     __shared__ int32_t s_ids[kMaxIds];
-    __shared__ uint8_t s_uidx[kMaxIds];
-    __shared__ uint32_t s_taken[kMaxRows][MOE_MAX_EXPERTS / 32];
+    __shared__ float s_wts[kMaxIds];
+    __shared__ uint32_t s_mask[kMaxIds];
     __shared__ int s_last;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -321,73 +194,16 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     const int E = p.E, k = p.k;
     if (warp < p.rows) {
         const int r = warp;
-        const float *lg = p.ws.logits + (size_t)r * E;
-        uint32_t *taken = s_taken[r];
-        for (int i = lane; i < MOE_MAX_EXPERTS / 32; i += 32) taken[i] = 0u;
+        warp_topk_row(p.ws.logits + (size_t)r * E, p.bias, E, k, p.scoring, p.norm, p.rsf,
+                      s_ids + r * k, s_wts + r * k, lane);
         __syncwarp();
-        for (int j = 0; j < k; ++j) {
-            float bk = -INFINITY;
-            int bi = 0x7fffffff;
-            for (int e = lane; e < E; e += 32) {
-                if ((taken[e >> 5] >> (e & 31)) & 1u) continue;
-                const float l = ld_cg(lg + e);
-                float key = l;
-                if (p.scoring == MOE_SCORING_SIGMOID) key = 1.f / (1.f + expf(-l)) + p.bias[e];
-                if (key != key) key = -INFINITY;   // NaN ranks lowest
-                if (key > bk || (key == bk && e < bi)) {
-                    bk = key;
-                    bi = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-                if (ok > bk || (ok == bk && oi < bi)) {
-                    bk = ok;
-                    bi = oi;
-                }
-            }
-            if (lane == 0) {
-                taken[bi >> 5] |= 1u << (bi & 31);
-                s_ids[r * k + j] = bi;
-            }
-            __syncwarp();
-        }
-        // routing weights of the k selected experts
-        const float top = ld_cg(lg + s_ids[r * k]);
-        float val[2] = {0.f, 0.f};
-        double part = 0.0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int j = lane + 32 * h;
-            if (j < k) {
-                const float l = ld_cg(lg + s_ids[r * k + j]);
-                val[h] = (p.scoring == MOE_SCORING_SOFTMAX) ? expf(l - top)
-                                                            : 1.f / (1.f + expf(-l));
-                part += (double)val[h];
-            }
-        }
-        double denom = 1.0;
-        if (p.norm) {
-            denom = warp_sum_d(part);
-        } else if (p.scoring == MOE_SCORING_SOFTMAX) {
-            double z = 0.0;
-            for (int e = lane; e < E; e += 32) z += (double)expf(ld_cg(lg + e) - top);
-            denom = warp_sum_d(z);
-        }
-        const double scale = (p.scoring == MOE_SCORING_SIGMOID) ? (double)p.rsf : 1.0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int j = lane + 32 * h;
-            if (j < k) {
-                const float w = (float)((double)val[h] / denom * scale);
-                const int id = s_ids[r * k + j];
-                p.ws.ids[r * k + j] = id;
-                p.ws.wts[r * k + j] = w;
-                if (p.ids_out) p.ids_out[r * k + j] = id;
-                if (p.wts_out) p.wts_out[r * k + j] = w;
-            }
+        for (int j = lane; j < k; j += 32) {
+            const int id = s_ids[r * k + j];
+            const float w = s_wts[r * k + j];
+            p.ws.ids[r * k + j] = id;
+            p.ws.wts[r * k + j] = w;
+            if (p.ids_out) p.ids_out[r * k + j] = id;
+            if (p.wts_out) p.wts_out[r * k + j] = w;
         }
     }
     if (threadIdx.x < kMaxRows && !(p.has_shared && p.shared_gated))
@@ -396,7 +212,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     if (p.do_union && warp == 0) {
         UnionSrc src{E,      k,      p.rows, p.per_row_mode, 1,        p.has_shared,
                      p.gate, p.up,   p.down, p.sh_gate,      p.sh_up, p.sh_down};
-        build_union(src, s_ids, s_uidx, p.ws.uni, p.ws.ptrs, p.ws.hdr, lane);
+        build_union(src, s_ids, s_mask, p.ws.uni, p.ws.ptrs, p.ws.hdr, lane);
     }
     if (threadIdx.x == 0) p.ws.hdr->route_ticket = 0u;
 }
@@ -407,7 +223,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 
 __global__ void __launch_bounds__(32) moe_union_kernel(const UnionParams p) {
     __shared__ int32_t s_ids[kMaxIds];
-    __shared__ uint8_t s_uidx[kMaxIds];
+    __shared__ uint32_t s_mask[kMaxIds];
     const int lane = threadIdx.x;
     pdl_wait();
     const int n = p.rows * p.k;
@@ -415,7 +231,7 @@ __global__ void __launch_bounds__(32) moe_union_kernel(const UnionParams p) {
     __syncwarp();
     UnionSrc src{p.E,    p.k,    p.rows, p.per_row_mode, p.has_tables, p.has_shared,
                  p.gate, p.up,   p.down, p.sh_gate,      p.sh_up,      p.sh_down};
-    build_union(src, s_ids, s_uidx, p.ws.uni, p.ws.ptrs, p.ws.hdr, lane);
+    build_union(src, s_ids, s_mask, p.ws.uni, p.ws.ptrs, p.ws.hdr, lane);
     __syncwarp();
     if (p.out) {
         const uint32_t *s = reinterpret_cast<const uint32_t *>(p.ws.uni);

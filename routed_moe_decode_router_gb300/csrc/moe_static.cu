@@ -61,8 +61,9 @@ extern "C" moe_status moe_forward_static(const moe_config *cfg, const moe_weight
     }
     void *ws = nullptr;
     if ((s = static_ws_address(&ws)) != MOE_OK) return s;
-    // The status word and the arrival counters must start at zero; the rest
-    // of the scratch is written before it is read.
+    // The status word and the grid-barrier counter (the workspace header)
+    // must start at zero; the rest of the scratch is written before it is
+    // read.
     cudaError_t e = cudaMemsetAsync(ws, 0, L.ids, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return moe::set_error(MOE_ERR_CUDA, cudaGetErrorString(e));
     return moe_forward(cfg, w, x, out, rows, ws, kStaticWsBytes, stream);

@@ -168,8 +168,9 @@ def moe_forward(cfg, w, x: int, out: int, rows: int, ws: int, ws_bytes: int,
 
 def moe_forward_timed(cfg, w, x: int, out: int, rows: int, ws: int,
                       ws_bytes: int, stream: int, events):
-    """events: four cudaEvent_t handles (ints)."""
-    arr = (C.c_void_p * 4)(*events)
+    """events: two cudaEvent_t handles (ints), recorded before and after the
+    layer kernel."""
+    arr = (C.c_void_p * 2)(*events)
     _check(lib().moe_forward_timed(C.byref(cfg), C.byref(w), x, out, rows, ws,
                                    ws_bytes, stream, arr))
 

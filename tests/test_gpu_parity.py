@@ -43,6 +43,12 @@ SMALL_SHAPES = {
     "h3072_maxc3": S(hidden=3072, num_experts=16, top_k=2, moe_inter=256, shared_inter=128),
     "i1536_down_w6": S(hidden=256, num_experts=16, top_k=4, moe_inter=1536, shared_inter=1536),
     "i4096_down_max": S(hidden=256, num_experts=8, top_k=2, moe_inter=4096, shared_inter=128),
+    "e1024_two_lists": S(hidden=256, num_experts=1024, top_k=8, moe_inter=128, shared_inter=128),
+    "e600_sigmoid_no_norm": S(hidden=384, num_experts=600, top_k=6, moe_inter=128,
+                              shared_inter=256, scoring="sigmoid", routed_scaling_factor=1.5,
+                              norm_topk_prob=False),
+    "e300_softmax_no_norm": S(hidden=256, num_experts=300, top_k=5, moe_inter=256,
+                              shared_inter=128, norm_topk_prob=False),
 }
 
 
