@@ -110,25 +110,29 @@ __device__ __forceinline__ void warp_topk_row_nk(const float *lg, const float *b
     float v[NL][NK];
 #pragma unroll
     for (int L = 0; L < NL; ++L) {
+        // every load of the list first (clamped index, no branch between
+        // them), so one memory latency covers the list
+        float bs[NK];
+#pragma unroll
+        for (int i = 0; i < NK; ++i) v[L][i] = ld_cg(lg + min(lane + 32 * (L * NK + i), E - 1));
+        if (sigm) {
+#pragma unroll
+            for (int i = 0; i < NK; ++i) bs[i] = bias[min(lane + 32 * (L * NK + i), E - 1)];
+        }
 #pragma unroll
         for (int i = 0; i < NK; ++i) {
             const int e = lane + 32 * (L * NK + i);
-            c[L][i] = 0ull;
-            v[L][i] = 0.f;
-            if (e < E) {
-                const float l = ld_cg(lg + e);
-                float kv;
-                if (sigm) {
-                    v[L][i] = 1.f / (1.f + expf(-l));
-                    kv = v[L][i] + bias[e];
-                } else {
-                    v[L][i] = l;
-                    kv = l;
-                }
-                if (kv != kv) kv = -INFINITY;   // NaN ranks lowest
-                kv += 0.f;                       // -0 ranks as +0
-                c[L][i] = pack_key_id(kv, e);
+            const float l = v[L][i];
+            float kv;
+            if (sigm) {
+                v[L][i] = 1.f / (1.f + expf(-l));
+                kv = v[L][i] + bs[i];
+            } else {
+                kv = l;
             }
+            if (kv != kv) kv = -INFINITY;   // NaN ranks lowest
+            kv += 0.f;                       // -0 ranks as +0
+            c[L][i] = e < E ? pack_key_id(kv, e) : 0ull;
         }
         sort_desc<NK>(c[L], v[L]);
     }
@@ -188,12 +192,24 @@ __device__ __forceinline__ void warp_topk_row_nk(const float *lg, const float *b
     } else if (!sigm) {
         // softmax without renormalisation: the full denominator over all E
         float zsum = 0.f, zerr = 0.f;
-        for (int e = lane; e < E; e += 32) {
-            float s, er;
-            two_sum(zsum, expf(ld_cg(lg + e) - top), s, er);
-            zsum = s;
-            zerr += er;
-        }
+#pragma unroll
+        for (int L = 0; L < NL; ++L)
+#pragma unroll
+            for (int i = 0; i < NK; ++i) {
+                // the unsorted logits are reloaded (L1/L2 hits), all loads first
+                const int e = lane + 32 * (L * NK + i);
+                v[L][i] = ld_cg(lg + min(e, E - 1));
+            }
+#pragma unroll
+        for (int L = 0; L < NL; ++L)
+#pragma unroll
+            for (int i = 0; i < NK; ++i) {
+                const int e = lane + 32 * (L * NK + i);
+                float s, er;
+                two_sum(zsum, e < E ? expf(v[L][i] - top) : 0.f, s, er);
+                zsum = s;
+                zerr += er;
+            }
         denom = warp_sum_compensated(zsum, zerr);
     }
 #pragma unroll
@@ -256,9 +272,12 @@ __device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, ui
         eq1 = 1u << lane;
     } else {
         eq0 = __match_any_sync(FULL, id0);
-        eq1 = __match_any_sync(FULL, id1);
+        eq1 = 1u << lane;   // positions >= n hold distinct negative ids
+        if (n > 32) {       // warp-uniform
+            eq1 = __match_any_sync(FULL, id1);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) cross |= (__shfl_sync(FULL, id0, q) == id1 ? 1u : 0u) << q;
+            for (int q = 0; q < 32; ++q) cross |= (__shfl_sync(FULL, id0, q) == id1 ? 1u : 0u) << q;
+        }
     }
     const bool first0 = p0 < n && (eq0 & below) == 0;
     const bool first1 = p1 < n && cross == 0 && (eq1 & below) == 0;
@@ -424,19 +443,29 @@ __device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_str
                                        float &inv1) {
     const int n = lane >> 2, q = lane & 3;
     const bool on = (mask >> n) & 1u;
+    // every load first, from a clamped address (row 0 when the row is off,
+    // the last chunk when the chunk is past the end), then zero the unused
+    const int nrow = on ? n : 0;
 #pragma unroll
     for (int m = 0; m < MAXC; ++m) {
-        const int c = warp + nwarps * m;
-        const bool live = on && c < nchunk;
-        const uint16_t *src = rows_base + (size_t)n * row_stride + c * kChunk + q * 32;
+        const int c = min(warp + nwarps * m, nchunk - 1);
+        const uint16_t *src = rows_base + (size_t)nrow * row_stride + c * kChunk + q * 32;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-            uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-            if (live) xv = ld_cg_v4(src + 8 * v);
+            const uint4 xv = ld_cg_v4(src + 8 * v);
             b[m][2 * v][0] = xv.x;
             b[m][2 * v][1] = xv.y;
             b[m][2 * v + 1][0] = xv.z;
             b[m][2 * v + 1][1] = xv.w;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < MAXC; ++m) {
+        const bool live = on && warp + nwarps * m < nchunk;
+#pragma unroll
+        for (int s2 = 0; s2 < 8; ++s2) {
+            b[m][s2][0] = live ? b[m][s2][0] : 0u;
+            b[m][s2][1] = live ? b[m][s2][1] : 0u;
         }
     }
     float mx = 0.f;
@@ -465,13 +494,28 @@ __device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_str
 
 // D fragment (lane g, q: rows g / g+8, columns 2q / 2q+1) -> smem, column
 // major [8 columns][16 rows], so that a column's 16 rows are contiguous.
+// Index of (column col, row r) in a warp's 16-row x 8-column block of
+// partial sums: column-major, rows XOR-swizzled in groups of four by the
+// column pair, so the compute warps' scattered stores hit half as many banks
+// twice and the epilogue's float4 reads (four rows of one column) stay
+// contiguous and conflict-free.
+__device__ __forceinline__ int partial_index(int col, int r) {
+    return col * 16 + (r ^ (4 * ((col >> 1) & 3)));
+}
+
+// The MMA accumulator of one 16 x 8 tile (rows g and g + 8, columns 2q and
+// 2q + 1) into a partial-sum block, undoing the column scales.
 __device__ __forceinline__ void store_partial(float *dst, const float (&d)[4], int g, int q,
                                               float inv0, float inv1) {
-    dst[(2 * q) * 16 + g] = d[0] * inv0;
-    dst[(2 * q + 1) * 16 + g] = d[1] * inv1;
-    dst[(2 * q) * 16 + g + 8] = d[2] * inv0;
-    dst[(2 * q + 1) * 16 + g + 8] = d[3] * inv1;
+    dst[partial_index(2 * q, g)] = d[0] * inv0;
+    dst[partial_index(2 * q + 1, g)] = d[1] * inv1;
+    dst[partial_index(2 * q, g + 8)] = d[2] * inv0;
+    dst[partial_index(2 * q + 1, g + 8)] = d[3] * inv1;
 }
+
+// SiLU with the fast exponential and division (relative error about 1e-6,
+// far below the bf16 rounding of the value it feeds).
+__device__ __forceinline__ float silu(float x) { return __fdividef(x, 1.f + __expf(-x)); }
 
 // ---------------------------------------------------------------------------
 // Stage ring wait and grid barrier, both bounded

@@ -101,28 +101,38 @@ size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
     return kLayerSmemFixed + (size_t)stages * slot_bytes + 2 * sizeof(uint64_t) * stages;
 }
 
-// Router weights of row `row` (E = the shared-expert gate vector) at the
-// 8 inputs h0..h0+7, as fp32 (NVFP4: e2m1 * e4m3; scale2 comes later).
-__device__ __forceinline__ void router_weights(const LayerParams &p, int row, int h0, float (&w)[8]) {
+// Raw router weights of row `row` (E = the shared-expert gate vector) at the
+// 8 inputs h0..h0+7: a uint4 of bf16 values, or (NVFP4) the packed word in
+// .x and the E4M3 scale byte in .y.  Loads only, so that several rows' loads
+// can be in flight before any is used.
+__device__ __forceinline__ uint4 router_raw(const LayerParams &p, int row, int h0) {
     const int H = p.H;
     if (row == p.E || p.router_fmt == MOE_ROUTER_BF16) {
         const uint16_t *src = (row == p.E) ? p.sh_vec + h0 : p.router_bf16 + (size_t)row * H + h0;
-        const uint4 v = ld_nc_v4(src);
+        return ld_nc_v4(src);
+    }
+    uint4 r;
+    r.x = *reinterpret_cast<const uint32_t *>(p.router_fp4.packed + (size_t)row * (H / 2) + h0 / 2);
+    r.y = p.router_fp4.scales[(size_t)row * (H / 16) + h0 / 16];
+    r.z = r.w = 0u;
+    return r;
+}
+
+// The 8 weights of router_raw as fp32 (NVFP4: e2m1 * e4m3; scale2 comes later).
+__device__ __forceinline__ void router_decode(const LayerParams &p, int row, uint4 v, float (&w)[8]) {
+    if (row == p.E || p.router_fmt == MOE_ROUTER_BF16) {
         w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
         w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
     } else {
-        const uint32_t pk = *reinterpret_cast<const uint32_t *>(p.router_fp4.packed +
-                                                                (size_t)row * (H / 2) + h0 / 2);
-        const uint32_t sc = p.router_fp4.scales[(size_t)row * (H / 16) + h0 / 16];
-        const uint32_t sh = e4m3x2_to_f16x2(sc);
-        const float s = __low2float(*reinterpret_cast<const __half2 *>(&sh));
+        const uint32_t sh = e4m3x2_to_f16x2(v.y);
+        const float sc = __low2float(*reinterpret_cast<const __half2 *>(&sh));
         uint32_t hq[4];
-        e2m1x8_to_f16x2(pk, hq);
+        e2m1x8_to_f16x2(v.x, hq);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const __half2 qv = *reinterpret_cast<const __half2 *>(&hq[i]);
-            w[2 * i] = __low2float(qv) * s;
-            w[2 * i + 1] = __high2float(qv) * s;
+            w[2 * i] = __low2float(qv) * sc;
+            w[2 * i + 1] = __high2float(qv) * sc;
         }
     }
 }
@@ -266,17 +276,24 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             for (int seg = warp; seg < nseg; seg += kConsumerWarps) {
                 const int h0 = seg * 256 + lane * 8;
                 const bool live = h0 < H;   // H is a multiple of 128, not always of 256
+                const int hc = live ? h0 : 0;
+                // every load first, from clamped addresses; unused values are zeroed after
                 uint4 xv[kMaxRows];
 #pragma unroll
                 for (int r = 0; r < kMaxRows; ++r)
-                    xv[r] = (live && r < p.rows) ? ld_cg_v4(p.x + (size_t)r * H + h0)
-                                                 : make_uint4(0u, 0u, 0u, 0u);
+                    if (r < p.rows) xv[r] = ld_cg_v4(p.x + (size_t)r * H + hc);
+                uint4 rv[kRouterRowsPerPass];
+#pragma unroll
+                for (int ri = 0; ri < kRouterRowsPerPass; ++ri)
+                    rv[ri] = router_raw(p, b + (r0 + min(ri, nr - 1)) * G, hc);
+#pragma unroll
+                for (int r = 0; r < kMaxRows; ++r)
+                    if (!live || r >= p.rows) xv[r] = make_uint4(0u, 0u, 0u, 0u);
                 float wv[kRouterRowsPerPass][8];
 #pragma unroll
                 for (int ri = 0; ri < kRouterRowsPerPass; ++ri) {
-                    if (live && ri < nr) {
-                        router_weights(p, b + (r0 + ri) * G, h0, wv[ri]);
-                    } else {
+                    router_decode(p, b + (r0 + min(ri, nr - 1)) * G, rv[ri], wv[ri]);
+                    if (!live || ri >= nr) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) wv[ri][i] = 0.f;
                     }
@@ -326,6 +343,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     MOE_PHASE_MARK(tid == 0, 3);
 
     // ---------------- phase B: top-k and union, in every CTA ----------------
+    // One warp per token row selects its experts; then the epilogue warp
+    // builds the union and loads the union experts' pointer entries while
+    // the compute warps load their token-row fragments, and publishes both
+    // through named barrier 4.
     if (is_epi && lane < kMaxRows)
         sm.gate_val[lane] = !p.has_shared ? 0.f : (gate_row ? ld_cg(p.ws.gate_val + lane) : 1.f);
     MOE_TIC(t_topk);
@@ -334,37 +355,46 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                       sm.ids + warp * k, sm.wts + warp * k, lane);
     MOE_TOC(tid == 0, 16, t_topk);
     __syncthreads();
-    MOE_TIC(t_union);
-    if (warp == 0) {
+    if (is_epi) {
+        MOE_TIC(t_union);
         UnionSrc src{E,      k,      p.rows, p.per_row_mode, 0,        p.has_shared,
                      p.gate, p.up,   p.down, p.sh_gate,      p.sh_up, p.sh_down};
         build_union(src, sm.ids, sm.umask, &sm.uni, sm.ptrs, hdr, lane);
-    }
-    MOE_TOC(tid == 0, 17, t_union);
-    __syncthreads();
-    MOE_PHASE_MARK(tid == 0, 4);
-    const int U = sm.uni.num_union;
-    if (b == 0) {   // publish the routing for moe_read_routing
-        const int n = p.rows * k;
-        for (int i = tid; i < n; i += blockDim.x) {
-            p.ws.ids[i] = sm.ids[i];
-            p.ws.wts[i] = sm.wts[i];
+        __syncwarp();
+        const moe_expert_table tabs[3] = {p.gate, p.up, p.down};
+        load_union_ptrs(&sm.uni, sm.uni.num_union, E, tabs, sm.ptrs, hdr, lane);
+        __syncwarp();
+        asm volatile("bar.arrive 4, %0;" ::"r"(kLayerThreads) : "memory");
+        MOE_TOC(lane == 0, 17, t_union);
+        MOE_PHASE_MARK(lane == 0, 4);
+        if (b == 0) {   // publish the routing for moe_read_routing
+            const int n = p.rows * k;
+            for (int i = lane; i < n; i += 32) {
+                p.ws.ids[i] = sm.ids[i];
+                p.ws.wts[i] = sm.wts[i];
+            }
+            const uint32_t *su = reinterpret_cast<const uint32_t *>(&sm.uni);
+            uint32_t *du = reinterpret_cast<uint32_t *>(p.ws.uni);
+            for (int i = lane; i < (int)(sizeof(moe_union_table) / 4); i += 32) du[i] = su[i];
+            if (lane < kMaxRows && !gate_row) p.ws.gate_val[lane] = sm.gate_val[lane];
         }
-        const uint32_t *su = reinterpret_cast<const uint32_t *>(&sm.uni);
-        uint32_t *du = reinterpret_cast<uint32_t *>(p.ws.uni);
-        for (int i = tid; i < (int)(sizeof(moe_union_table) / 4); i += blockDim.x) du[i] = su[i];
-        if (tid < kMaxRows && !gate_row) p.ws.gate_val[tid] = sm.gate_val[tid];
+    } else if (is_prod) {
+        named_bar(4, kLayerThreads);
     }
-    const int Tgu = St + U * It;
-    const int Td = Sd + U * Ho;
-    const int d_begin = (int)((long long)b * Td / G);
-    const int d_end = (int)((long long)(b + 1) * Td / G);
+    // (the compute warps pass barrier 4 after loading their fragments)
+    const uint32_t allrows = (1u << p.rows) - 1u;
+    int U = 0, Tgu = 0, Td = 0, d_begin = 0, d_end = 0;
+    auto sweep_layout = [&]() {
+        U = sm.uni.num_union;
+        Tgu = St + U * It;
+        Td = Sd + U * Ho;
+        d_begin = (int)((long long)b * Td / G);
+        d_end = (int)((long long)(b + 1) * Td / G);
+    };
 
     // ---------------- producer: pointer table, then every remaining slot ----------------
     if (is_prod) {
-        const moe_expert_table tabs[3] = {p.gate, p.up, p.down};
-        load_union_ptrs(&sm.uni, U, E, tabs, sm.ptrs, hdr, lane);
-        __syncwarp();
+        sweep_layout();
         if (lane == 0) {
             bool ok = true;
             for (; ok && pj < Tgu; pj += G) ok = issue_gu(pj);
@@ -394,22 +424,22 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         return;
     }
 
-    const uint32_t allrows = (1u << p.rows) - 1u;
-
     if (is_epi) {
         // ---------------- epilogue warp ----------------
+        // Everything a unit's epilogue needs except the partial sums (entry,
+        // tile, scales, row mask, destination) is fetched before waiting for
+        // them, and the eight warps' partials are loaded unconditionally and
+        // summed with a select, so one shared-memory latency covers them.
+        sweep_layout();
         int ui = 0;
         const int nwg = min(kConsumerWarps, H / kChunk);   // warps holding gate/up partials
+        const int col = lane >> 2, rq = lane & 3;
         for (int j = b; j < Tgu; j += G, ++ui) {
             const int rb = ui % kRed;
-            MOE_TIC(t_ew);
-            ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
-            MOE_TOC(lane == 0, 25, t_ew);
-            MOE_TIC(t_ex);
             int entry, tile;
             float s2g, s2u;
             uint32_t mask;
-            bool valid = !*abort;
+            bool live = true;
             if (j < St) {
                 entry = kSharedEntry;
                 tile = j;
@@ -419,46 +449,51 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             } else {
                 entry = (j - St) / It;
                 tile = (j - St) % It;
-                valid = valid && sm.ptrs[entry].expert >= 0;
+                live = sm.ptrs[entry].expert >= 0;
                 s2g = sm.ptrs[entry].scale2[0];
                 s2u = sm.ptrs[entry].scale2[1];
                 mask = sm.uni.rowmask[entry];
             }
-            // lane: column col = lane / 4, rows r0..r0+3 (r0 = 4 * (lane % 4))
-            {
-                const int col = lane >> 2, r0 = (lane & 3) * 4;
-                float4 gs = make_float4(0.f, 0.f, 0.f, 0.f), us = gs;
+            live = live && ((mask >> col) & 1u);
+            // lane: column col, rows 4 * rq .. + 3 of the 16-row tile
+            const int off = partial_index(col, 4 * rq);
+            MOE_TIC(t_ew);
+            ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
+            MOE_TOC(lane == 0, 25, t_ew);
+            MOE_TIC(t_ex);
+            float4 ga[kConsumerWarps], ua[kConsumerWarps];
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    if (w < nwg) {
-                        const float4 a =
-                            *reinterpret_cast<const float4 *>(&sm.red[rb][w][col * 16 + r0]);
-                        const float4 c =
-                            *reinterpret_cast<const float4 *>(&sm.red[rb][w][128 + col * 16 + r0]);
-                        gs.x += a.x; gs.y += a.y; gs.z += a.z; gs.w += a.w;
-                        us.x += c.x; us.y += c.y; us.z += c.z; us.w += c.w;
-                    }
-                }
-                if (valid && ((mask >> col) & 1u)) {
-                    const float g4[4] = {gs.x, gs.y, gs.z, gs.w}, u4[4] = {us.x, us.y, us.z, us.w};
-                    uint32_t hv[2];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        float h2[2];
-#pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            const float gv = g4[2 * i + z] * s2g, uv = u4[2 * i + z] * s2u;
-                            h2[z] = gv / (1.f + expf(-gv)) * uv;
-                        }
-                        hv[i] = (uint32_t)f2bf16_rn(h2[0]) | ((uint32_t)f2bf16_rn(h2[1]) << 16);
-                    }
-                    *reinterpret_cast<uint2 *>(p.ws.hbuf +
-                                               ((size_t)entry * kMaxRows + col) * p.ws.inter_max +
-                                               tile * kTileRows + r0) = make_uint2(hv[0], hv[1]);
-                }
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                ga[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][off]);
+                ua[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][128 + off]);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.red_empty[rb]);
+            if (lane == 0) mbar_arrive(&sm.red_empty[rb]);   // the values are in registers
+            float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const bool on = w < nwg;
+                gs[0] += on ? ga[w].x : 0.f; gs[1] += on ? ga[w].y : 0.f;
+                gs[2] += on ? ga[w].z : 0.f; gs[3] += on ? ga[w].w : 0.f;
+                us[0] += on ? ua[w].x : 0.f; us[1] += on ? ua[w].y : 0.f;
+                us[2] += on ? ua[w].z : 0.f; us[3] += on ? ua[w].w : 0.f;
+            }
+            if (live && !*abort) {
+                uint32_t hv[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    float h2[2];
+#pragma unroll
+                    for (int z = 0; z < 2; ++z) {
+                        const float gv = gs[2 * i + z] * s2g, uv = us[2 * i + z] * s2u;
+                        h2[z] = silu(gv) * uv;
+                    }
+                    hv[i] = (uint32_t)f2bf16_rn(h2[0]) | ((uint32_t)f2bf16_rn(h2[1]) << 16);
+                }
+                *reinterpret_cast<uint2 *>(p.ws.hbuf +
+                                           ((size_t)entry * kMaxRows + col) * p.ws.inter_max +
+                                           tile * kTileRows + 4 * rq) = make_uint2(hv[0], hv[1]);
+            }
             MOE_TOC(lane == 0, 26, t_ex);
         }
         // every h of this CTA is stored: grid barrier, then release the compute warps
@@ -468,16 +503,14 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         __syncwarp();
         MOE_PHASE_MARK(lane == 0, 14);
         asm volatile("bar.arrive 2, %0;" ::"r"(kComputeAndEpi) : "memory");
+        // lane: column col, rows 8 * (rq & 1) .. + 7 of MMA tile rq >> 1
+        const int half = rq >> 1, r0 = (rq & 1) * 8;
         for (int j = d_begin; j < d_end; ++j, ++ui) {
             const int rb = ui % kRed;
-            MOE_TIC(t_ew);
-            ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
-            MOE_TOC(lane == 0, 27, t_ew);
-            MOE_TIC(t_ex);
             int entry, tile, K;
             uint32_t mask;
             float s2;
-            bool valid = !*abort;
+            bool live = true;
             if (j < Sd) {
                 entry = kSharedEntry;
                 tile = j;
@@ -489,38 +522,44 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 tile = (j - Sd) % Ho;
                 K = p.I;
                 mask = sm.uni.rowmask[entry];
-                valid = valid && sm.ptrs[entry].expert >= 0;
+                live = sm.ptrs[entry].expert >= 0;
                 s2 = sm.ptrs[entry].scale2[2];
             }
+            live = live && ((mask >> col) & 1u);
             const int nwd = min(kConsumerWarps, K / kChunk);   // warps holding down partials
-            // lane: column col = lane / 4, unit rows 8 * (lane % 4) .. + 7
-            {
-                const int col = lane >> 2, rg = lane & 3;
-                const int half = rg >> 1, r0 = (rg & 1) * 8;   // MMA tile, first row in it
-                float ys[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            const int o = tile * kOutTile + half * kTileRows + r0;
+            float *dst = (entry == kSharedEntry)
+                             ? p.ws.ysbuf + (size_t)col * H + o
+                             : p.ws.ybuf + ((size_t)col * k + (live ? sm.uni.uslot[entry][col] : 0)) * H + o;
+            const int off0 = half * 128 + partial_index(col, r0);
+            const int off1 = half * 128 + partial_index(col, r0 + 4);
+            MOE_TIC(t_ew);
+            ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
+            MOE_TOC(lane == 0, 27, t_ew);
+            MOE_TIC(t_ex);
+            float4 a[kConsumerWarps], c[kConsumerWarps];
 #pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    if (w < nwd) {
-                        const float *src = &sm.red[rb][w][half * 128 + col * 16 + r0];
-                        const float4 a = *reinterpret_cast<const float4 *>(src);
-                        const float4 c = *reinterpret_cast<const float4 *>(src + 4);
-                        ys[0] += a.x; ys[1] += a.y; ys[2] += a.z; ys[3] += a.w;
-                        ys[4] += c.x; ys[5] += c.y; ys[6] += c.z; ys[7] += c.w;
-                    }
-                }
-                if (valid && ((mask >> col) & 1u)) {
-                    const int o = tile * kOutTile + half * kTileRows + r0;
-                    float *dst = (entry == kSharedEntry)
-                                     ? p.ws.ysbuf + (size_t)col * H + o
-                                     : p.ws.ybuf + ((size_t)col * k + sm.uni.uslot[entry][col]) * H + o;
-                    *reinterpret_cast<float4 *>(dst) =
-                        make_float4(ys[0] * s2, ys[1] * s2, ys[2] * s2, ys[3] * s2);
-                    *reinterpret_cast<float4 *>(dst + 4) =
-                        make_float4(ys[4] * s2, ys[5] * s2, ys[6] * s2, ys[7] * s2);
-                }
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                a[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][off0]);
+                c[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][off1]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.red_empty[rb]);
+            float ys[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const bool on = w < nwd;
+                ys[0] += on ? a[w].x : 0.f; ys[1] += on ? a[w].y : 0.f;
+                ys[2] += on ? a[w].z : 0.f; ys[3] += on ? a[w].w : 0.f;
+                ys[4] += on ? c[w].x : 0.f; ys[5] += on ? c[w].y : 0.f;
+                ys[6] += on ? c[w].z : 0.f; ys[7] += on ? c[w].w : 0.f;
+            }
+            if (live && !*abort) {
+                *reinterpret_cast<float4 *>(dst) =
+                    make_float4(ys[0] * s2, ys[1] * s2, ys[2] * s2, ys[3] * s2);
+                *reinterpret_cast<float4 *>(dst + 4) =
+                    make_float4(ys[4] * s2, ys[5] * s2, ys[6] * s2, ys[7] * s2);
+            }
             MOE_TOC(lane == 0, 28, t_ex);
         }
         __syncwarp();
@@ -551,6 +590,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             load_b<MC_GU>(p.x, (size_t)H, allrows, H / kChunk, warp, kConsumerWarps, lane, bx,
                           inv0, inv1);
             MOE_PHASE_MARK(tid == 0, 5);
+            named_bar(4, kLayerThreads);
+            sweep_layout();
             const int nch = H / kChunk;
             for (int j = b; j < Tgu; j += G) {
                 const int s0 = ci % S, s1 = (ci + 1) % S;
@@ -677,10 +718,19 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     for (int it = b + G * warp; it < items; it += G * (kConsumerWarps + 1)) {
         const int t = it / p.rows, r = it % p.rows;
         const int o = t * kOutTile + lane;
+        const float ysv = ld_cg(p.ws.ysbuf + (size_t)r * H + o);
         float acc = 0.f;
-        for (int sl = 0; sl < k; ++sl)
-            acc = fmaf(sm.wts[r * k + sl], ld_cg(p.ws.ybuf + ((size_t)r * k + sl) * H + o), acc);
-        if (p.has_shared) acc = fmaf(sm.gate_val[r], ld_cg(p.ws.ysbuf + (size_t)r * H + o), acc);
+        // slots in order, eight loads in flight at a time
+        for (int s0 = 0; s0 < k; s0 += 8) {
+            float yv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                yv[i] = ld_cg(p.ws.ybuf + ((size_t)r * k + min(s0 + i, k - 1)) * H + o);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (s0 + i < k) acc = fmaf(sm.wts[r * k + s0 + i], yv[i], acc);
+        }
+        if (p.has_shared) acc = fmaf(sm.gate_val[r], ysv, acc);
         if (!*abort) p.out[(size_t)r * H + o] = f2bf16_rn(acc);
     }
     MOE_PHASE_MARK(tid == 0, 9);
