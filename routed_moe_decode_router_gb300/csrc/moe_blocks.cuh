@@ -40,14 +40,6 @@ __device__ __forceinline__ bool aligned16(const void *p) {
 // over the selected slots when norm_topk_prob, times routed_scaling_factor.
 // All arithmetic is fp32 (expf, IEEE division); the sums are compensated.
 
-// Orderable 64-bit form of (key, id): larger key first, then lower id.
-// Any real key packs above 0, the value of an empty candidate.
-__device__ __forceinline__ unsigned long long pack_key_id(float key, int id) {
-    uint32_t u = __float_as_uint(key);
-    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // monotone float -> uint
-    return ((unsigned long long)u << 32) | (uint32_t)(0x7fffffff - id);
-}
-
 // Error-free sum a + b = s + e (Knuth's TwoSum).
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     s = a + b;
@@ -70,104 +62,70 @@ __device__ __forceinline__ float warp_sum_compensated(float v, float c) {
     return v + c;
 }
 
-// Descending bitonic sort of NK packed candidates (values carried along).
-template <int NK>
-__device__ __forceinline__ void sort_desc(unsigned long long (&c)[NK], float (&v)[NK]) {
-#pragma unroll
-    for (int size = 2; size <= NK; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-#pragma unroll
-            for (int i = 0; i < NK; ++i) {
-                const int j = i ^ stride;
-                if (j > i) {
-                    const bool desc = (i & size) == 0;
-                    const bool sw = desc ? (c[i] < c[j]) : (c[i] > c[j]);
-                    const unsigned long long ci = c[i], cj = c[j];
-                    const float vi = v[i], vj = v[j];
-                    c[i] = sw ? cj : ci;
-                    c[j] = sw ? ci : cj;
-                    v[i] = sw ? vj : vi;
-                    v[j] = sw ? vi : vj;
-                }
-            }
-        }
-    }
-}
-
-// Each lane holds NL sorted lists of NK candidates (experts
-// lane + 32 * (list * NK + i)), so E <= 32 * NK * NL; the keys are loaded
-// once.  Every selection is two warp max reductions (key, then the lowest id
-// among equal keys) over the lanes' best heads and a shift of the winner's
-// list.
+// Each lane holds the keys of experts lane + 32 * i (i < NK * NL, so
+// E <= 32 * NK * NL) in registers, loaded once.  A selection round takes
+// every lane's best key with an fp32 max tree, the warp's best with one
+// unsigned max reduction over an order-preserving form of the key, and the
+// lowest expert id holding it with one unsigned min reduction; the lane
+// holding that expert retires it (its key becomes NaN, which fmaxf skips).
+// No sort and no predicate chains, so the rounds are short.
 template <int NK, int NL>
 __device__ __forceinline__ void warp_topk_row_nk(const float *lg, const float *bias, int E, int k,
                                                  int scoring, int norm, float rsf,
                                                  int32_t *ids_out, float *wts_out, int lane) {
     const unsigned FULL = 0xffffffffu;
     const bool sigm = scoring == MOE_SCORING_SIGMOID;
-    unsigned long long c[NL][NK];
-    float v[NL][NK];
+    constexpr int N = NK * NL;   // candidates per lane: experts lane + 32 * i
+    float key[N], v[N];
+    // every load first (clamped index, no branch between them), so one
+    // memory latency covers them
 #pragma unroll
-    for (int L = 0; L < NL; ++L) {
-        // every load of the list first (clamped index, no branch between
-        // them), so one memory latency covers the list
-        float bs[NK];
+    for (int i = 0; i < N; ++i) v[i] = ld_cg(lg + min(lane + 32 * i, E - 1));
+    if (sigm) {
 #pragma unroll
-        for (int i = 0; i < NK; ++i) v[L][i] = ld_cg(lg + min(lane + 32 * (L * NK + i), E - 1));
+        for (int i = 0; i < N; ++i) key[i] = bias[min(lane + 32 * i, E - 1)];
+    }
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        float kv;
         if (sigm) {
-#pragma unroll
-            for (int i = 0; i < NK; ++i) bs[i] = bias[min(lane + 32 * (L * NK + i), E - 1)];
+            v[i] = 1.f / (1.f + expf(-v[i]));
+            kv = v[i] + key[i];
+        } else {
+            kv = v[i];
         }
-#pragma unroll
-        for (int i = 0; i < NK; ++i) {
-            const int e = lane + 32 * (L * NK + i);
-            const float l = v[L][i];
-            float kv;
-            if (sigm) {
-                v[L][i] = 1.f / (1.f + expf(-l));
-                kv = v[L][i] + bs[i];
-            } else {
-                kv = l;
-            }
-            if (kv != kv) kv = -INFINITY;   // NaN ranks lowest
-            kv += 0.f;                       // -0 ranks as +0
-            c[L][i] = e < E ? pack_key_id(kv, e) : 0ull;
-        }
-        sort_desc<NK>(c[L], v[L]);
+        if (kv != kv) kv = -INFINITY;   // a NaN key ranks lowest
+        kv += 0.f;                       // -0 ranks as +0
+        // NaN marks an empty candidate: fmaxf ignores it and it equals nothing
+        key[i] = lane + 32 * i < E ? kv : __int_as_float(0x7fffffff);
     }
     int my_id0 = 0, my_id1 = 0;     // expert of slots lane and lane + 32
     float my_v0 = 0.f, my_v1 = 0.f; // its logit (softmax) or sigmoid (sigmoid scoring)
     for (int j = 0; j < k; ++j) {
-        int from = 0;
-        unsigned long long head = c[0][0];
-        float hv = v[0][0];
+        // this lane's best key (a max tree, no predicates)
+        float m = key[0];
 #pragma unroll
-        for (int L = 1; L < NL; ++L) {
-            if (c[L][0] > head) {
-                head = c[L][0];
-                hv = v[L][0];
-                from = L;
-            }
+        for (int i = 1; i < N; ++i) m = fmaxf(m, key[i]);
+        // order-preserving unsigned form; an all-empty lane (NaN) maps to 0
+        uint32_t u = __float_as_uint(m);
+        u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+        u = (m != m) ? 0u : u;
+        const uint32_t mu = __reduce_max_sync(FULL, u);
+        const float mk = __uint_as_float((mu & 0x80000000u) ? (mu & 0x7fffffffu) : ~mu);
+        // the lowest expert id holding the best key (ties -> lower id)
+        uint32_t cand = 0xffffffffu;
+#pragma unroll
+        for (int i = N - 1; i >= 0; --i) cand = key[i] == mk ? (uint32_t)(lane + 32 * i) : cand;
+        const int bi = (int)__reduce_min_sync(FULL, cand);
+        // its value, from the lane that holds it; that lane retires it
+        float val = 0.f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const bool hit = lane + 32 * i == bi;
+            val = hit ? v[i] : val;
+            key[i] = hit ? __int_as_float(0x7fffffff) : key[i];
         }
-        const uint32_t hi = (uint32_t)(head >> 32), lo = (uint32_t)head;
-        const uint32_t mk = __reduce_max_sync(FULL, hi);
-        const uint32_t ml = __reduce_max_sync(FULL, hi == mk ? lo : 0u);
-        const int bi = 0x7fffffff - (int)ml;
-        const float bv = __shfl_sync(FULL, hv, bi & 31);
-        if (hi == mk && lo == ml) {   // the winner lane drops the head of its list
-#pragma unroll
-            for (int L = 0; L < NL; ++L) {
-                if (L == from) {
-#pragma unroll
-                    for (int i = 0; i + 1 < NK; ++i) {
-                        c[L][i] = c[L][i + 1];
-                        v[L][i] = v[L][i + 1];
-                    }
-                    c[L][NK - 1] = 0ull;
-                }
-            }
-        }
+        const float bv = __shfl_sync(FULL, val, bi & 31);
         if (lane == (j & 31)) {
             if (j < 32) {
                 my_id0 = bi;
@@ -192,24 +150,14 @@ __device__ __forceinline__ void warp_topk_row_nk(const float *lg, const float *b
     } else if (!sigm) {
         // softmax without renormalisation: the full denominator over all E
         float zsum = 0.f, zerr = 0.f;
+        // the logits again (the values were kept in v), in expert order
 #pragma unroll
-        for (int L = 0; L < NL; ++L)
-#pragma unroll
-            for (int i = 0; i < NK; ++i) {
-                // the unsorted logits are reloaded (L1/L2 hits), all loads first
-                const int e = lane + 32 * (L * NK + i);
-                v[L][i] = ld_cg(lg + min(e, E - 1));
-            }
-#pragma unroll
-        for (int L = 0; L < NL; ++L)
-#pragma unroll
-            for (int i = 0; i < NK; ++i) {
-                const int e = lane + 32 * (L * NK + i);
-                float s, er;
-                two_sum(zsum, e < E ? expf(v[L][i] - top) : 0.f, s, er);
-                zsum = s;
-                zerr += er;
-            }
+        for (int i = 0; i < N; ++i) {
+            float s, er;
+            two_sum(zsum, lane + 32 * i < E ? expf(v[i] - top) : 0.f, s, er);
+            zsum = s;
+            zerr += er;
+        }
         denom = warp_sum_compensated(zsum, zerr);
     }
 #pragma unroll
@@ -265,6 +213,14 @@ __device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, ui
     // unused positions get distinct negative ids, so they never match
     const int id0 = p0 < n ? s_ids[p0] : -1 - p0;
     const int id1 = p1 < n ? s_ids[p1] : -1 - p1;
+    // the pointer entries of both positions' experts are loaded first (from
+    // a clamped id), so their memory latency overlaps the scan below
+    PtrEntry pe[2];
+    if (src.has_tables) {
+        const moe_expert_table tb[3] = {src.gate, src.up, src.down};
+        load_ptr_entry(tb, min(max(id0, 0), src.E - 1), pe[0]);
+        if (n > 32) load_ptr_entry(tb, min(max(id1, 0), src.E - 1), pe[1]);
+    }
     const unsigned below = (1u << lane) - 1u;
     unsigned eq0, eq1, cross = 0;   // same-id lanes: half 0 for id0, half 1 for id1, half 0 for id1
     if (src.per_row_mode) {
@@ -324,8 +280,7 @@ __device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, ui
                 e = PtrEntry{};
                 e.expert = -1;
             } else {
-                const moe_expert_table tb[3] = {src.gate, src.up, src.down};
-                load_ptr_entry(tb, x, e);
+                e = pe[h];
                 bool ok = true;
 #pragma unroll
                 for (int m = 0; m < 3; ++m)
@@ -357,33 +312,6 @@ __device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, ui
         ut->top_k = src.k;
         ut->per_row_mode = src.per_row_mode;
         ut->num_union = U;
-    }
-}
-
-// Pointer entries of the union experts (entries u < U of `ut`), one lane per
-// entry, with the range and alignment checks of build_union; used when the
-// union was built without tables.  All 32 lanes of one warp call it.
-__device__ inline void load_union_ptrs(const moe_union_table *ut, int U, int E,
-                                       const moe_expert_table *tabs, PtrEntry *ptrs, WsHeader *hdr,
-                                       int lane) {
-    for (int u = lane; u < U; u += 32) {
-        const int x = ut->expert[u];
-        PtrEntry e;
-        if (x < 0 || x >= E) {
-            record_fault(hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)u);
-            e = PtrEntry{};
-            e.expert = -1;
-        } else {
-            load_ptr_entry(tabs, x, e);
-            bool ok = true;
-#pragma unroll
-            for (int m = 0; m < 3; ++m) ok = ok && aligned16(e.packed[m]) && aligned16(e.scales[m]);
-            if (!ok) {
-                record_fault(hdr, MOE_DEV_MISALIGNED_PTR, (uint32_t)x);
-                e.expert = -1;
-            }
-        }
-        ptrs[u] = e;
     }
 }
 

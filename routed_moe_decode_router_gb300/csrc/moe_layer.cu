@@ -344,8 +344,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
 
     // ---------------- phase B: top-k and union, in every CTA ----------------
     // One warp per token row selects its experts; then the epilogue warp
-    // builds the union and loads the union experts' pointer entries while
-    // the compute warps load their token-row fragments, and publishes both
+    // builds the union and the union experts' pointer entries while the
+    // compute warps load their token-row fragments, and publishes both
     // through named barrier 4.
     if (is_epi && lane < kMaxRows)
         sm.gate_val[lane] = !p.has_shared ? 0.f : (gate_row ? ld_cg(p.ws.gate_val + lane) : 1.f);
@@ -357,12 +357,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     __syncthreads();
     if (is_epi) {
         MOE_TIC(t_union);
-        UnionSrc src{E,      k,      p.rows, p.per_row_mode, 0,        p.has_shared,
+        UnionSrc src{E,      k,      p.rows, p.per_row_mode, 1,        p.has_shared,
                      p.gate, p.up,   p.down, p.sh_gate,      p.sh_up, p.sh_down};
         build_union(src, sm.ids, sm.umask, &sm.uni, sm.ptrs, hdr, lane);
-        __syncwarp();
-        const moe_expert_table tabs[3] = {p.gate, p.up, p.down};
-        load_union_ptrs(&sm.uni, sm.uni.num_union, E, tabs, sm.ptrs, hdr, lane);
         __syncwarp();
         asm volatile("bar.arrive 4, %0;" ::"r"(kLayerThreads) : "memory");
         MOE_TOC(lane == 0, 17, t_union);
