@@ -1,9 +1,10 @@
 // moe_layer.cu -- the whole routed MoE layer as one persistent kernel.
 //
-// One CTA per SM (every CTA resident at once): 8 compute warps, 1 epilogue
-// warp (cross-warp reductions and output stores, fed through a double buffer
-// of partial sums behind mbarriers, so the compute warps never wait for an
-// epilogue) and 1 producer warp (pointer table and bulk copies).  Phases:
+// One CTA per SM (every CTA resident at once): 8 compute warps, 2 epilogue
+// warps (cross-warp reductions and output stores; they take alternate units,
+// each fed through its own buffer of partial sums behind mbarriers, so the
+// compute warps rarely wait for an epilogue) and 1 producer warp (bulk
+// copies).  Phases:
 //   A  router: the E router rows (plus the shared-expert gate vector as row
 //      E) are spread over the CTAs; each row's dot products for all token
 //      rows are split over the compute warps (forward_token_major.rs:
@@ -76,10 +77,13 @@ namespace moe {
 constexpr int kRouterRowsPerPass = 4;     // router rows of one CTA handled together
 constexpr int kMaxSegs = MOE_MAX_HIDDEN / 256;
 constexpr int kRed = 2;                   // partial-sum buffers between compute and epilogue
-constexpr int kEpiWarp = kConsumerWarps;  // warp 8: reductions and output stores
+constexpr int kEpiWarp = kConsumerWarps;        // warp 8: first epilogue warp (and the union)
 constexpr int kProdWarp = kConsumerWarps + 1;   // warp 9: bulk-copy producer
-constexpr int kLayerThreads = (kConsumerWarps + 2) * 32;
-constexpr int kComputeAndEpi = (kConsumerWarps + 1) * 32;
+constexpr int kEpiWarp2 = kConsumerWarps + 2;   // warp 10: second epilogue warp
+constexpr int kEpiWarps = 2;                    // epilogue warp e takes units ui with ui % 2 == e
+constexpr int kLayerThreads = (kConsumerWarps + 3) * 32;
+constexpr int kComputeAndEpi = (kConsumerWarps + kEpiWarps) * 32;
+static_assert(kRed == kEpiWarps, "each epilogue warp owns one partial-sum buffer");
 
 struct LayerSmem {
     float red[kRed][kConsumerWarps][256];       // compute warps' partial sums
@@ -154,7 +158,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     const int Ho = H / kOutTile;                 // down units (32 rows) per entry
     const int Sd = p.has_shared ? Ho : 0;
     const bool is_comp = warp < kConsumerWarps;
-    const bool is_epi = warp == kEpiWarp;
+    const bool is_epi = warp == kEpiWarp || warp == kEpiWarp2;
+    const int epi_idx = warp == kEpiWarp2 ? 1 : 0;
     const bool is_prod = warp == kProdWarp;
     const bool gate_row = p.has_shared && p.shared_gated;
     const int nrow = E + (gate_row ? 1 : 0);
@@ -347,7 +352,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     // builds the union and the union experts' pointer entries while the
     // compute warps load their token-row fragments, and publishes both
     // through named barrier 4.
-    if (is_epi && lane < kMaxRows)
+    if (warp == kEpiWarp && lane < kMaxRows)
         sm.gate_val[lane] = !p.has_shared ? 0.f : (gate_row ? ld_cg(p.ws.gate_val + lane) : 1.f);
     MOE_TIC(t_topk);
     if (warp < p.rows)
@@ -355,7 +360,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                       sm.ids + warp * k, sm.wts + warp * k, lane);
     MOE_TOC(tid == 0, 16, t_topk);
     __syncthreads();
-    if (is_epi) {
+    if (warp == kEpiWarp) {
         MOE_TIC(t_union);
         UnionSrc src{E,      k,      p.rows, p.per_row_mode, 1,        p.has_shared,
                      p.gate, p.up,   p.down, p.sh_gate,      p.sh_up, p.sh_down};
@@ -375,7 +380,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             for (int i = lane; i < (int)(sizeof(moe_union_table) / 4); i += 32) du[i] = su[i];
             if (lane < kMaxRows && !gate_row) p.ws.gate_val[lane] = sm.gate_val[lane];
         }
-    } else if (is_prod) {
+    } else if (is_prod || warp == kEpiWarp2) {
         named_bar(4, kLayerThreads);
     }
     // (the compute warps pass barrier 4 after loading their fragments)
@@ -432,6 +437,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         const int nwg = min(kConsumerWarps, H / kChunk);   // warps holding gate/up partials
         const int col = lane >> 2, rq = lane & 3;
         for (int j = b; j < Tgu; j += G, ++ui) {
+            if ((ui & 1) != epi_idx) continue;
             const int rb = ui % kRed;
             int entry, tile;
             float s2g, s2u;
@@ -493,16 +499,18 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             }
             MOE_TOC(lane == 0, 26, t_ex);
         }
-        // every h of this CTA is stored: grid barrier, then release the compute warps
-        __syncwarp();
-        MOE_PHASE_MARK(lane == 0, 13);
-        if (lane == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 2u);
-        __syncwarp();
-        MOE_PHASE_MARK(lane == 0, 14);
+        // every h of this CTA is stored (both epilogue warps): grid barrier,
+        // then release the compute warps
+        named_bar(5, kEpiWarps * 32);
+        MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 13);
+        if (lane == 0 && epi_idx == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 2u);
+        named_bar(5, kEpiWarps * 32);
+        MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 14);
         asm volatile("bar.arrive 2, %0;" ::"r"(kComputeAndEpi) : "memory");
         // lane: column col, rows 8 * (rq & 1) .. + 7 of MMA tile rq >> 1
         const int half = rq >> 1, r0 = (rq & 1) * 8;
         for (int j = d_begin; j < d_end; ++j, ++ui) {
+            if ((ui & 1) != epi_idx) continue;
             const int rb = ui % kRed;
             int entry, tile, K;
             uint32_t mask;
@@ -559,10 +567,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             }
             MOE_TOC(lane == 0, 28, t_ex);
         }
-        __syncwarp();
-        MOE_PHASE_MARK(lane == 0, 15);
-        if (lane == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 3u);
-        __syncwarp();
+        named_bar(5, kEpiWarps * 32);
+        MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 15);
+        if (lane == 0 && epi_idx == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 3u);
+        named_bar(5, kEpiWarps * 32);   // both epilogue warps read y in the blend
         asm volatile("bar.arrive 3, %0;" ::"r"(kComputeAndEpi) : "memory");
     } else {
         // ---------------- compute warps ----------------
@@ -712,7 +720,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     // Items (32-row output tile, token row) go to the compute and epilogue
     // warps of all CTAs, one warp per item, one output per lane.
     const int items = Ho * p.rows;
-    for (int it = b + G * warp; it < items; it += G * (kConsumerWarps + 1)) {
+    const int bw = warp == kEpiWarp2 ? kConsumerWarps + 1 : warp;   // blend warp index
+    for (int it = b + G * bw; it < items; it += G * (kConsumerWarps + kEpiWarps)) {
         const int t = it / p.rows, r = it % p.rows;
         const int o = t * kOutTile + lane;
         const float ysv = ld_cg(p.ws.ysbuf + (size_t)r * H + o);
