@@ -575,8 +575,16 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     } else {
         // ---------------- compute warps ----------------
         const int g = lane >> 2, q = lane & 3;
-        int ci = 0;   // slots consumed
-        int ui = 0;   // units handed to the epilogue warp
+        int ci = 0;          // slots consumed
+        int rs = 0;          // ring slot of the next tile, and its phase parity
+        uint32_t rp = 0u;
+        auto next_slot = [&]() {
+            if (++rs == S) {
+                rs = 0;
+                rp ^= 1u;
+            }
+        };
+        int ui = 0;   // units handed to the epilogue warps
         // wait until the epilogue warp has consumed the buffer this unit reuses
         auto claim_red = [&]() -> int {
             const int rb = ui % kRed;
@@ -599,11 +607,15 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             sweep_layout();
             const int nch = H / kChunk;
             for (int j = b; j < Tgu; j += G) {
-                const int s0 = ci % S, s1 = (ci + 1) % S;
+                const int s0 = rs;
+                const uint32_t p0 = rp;
+                next_slot();
+                const int s1 = rs;
+                const uint32_t p1 = rp;
+                next_slot();
                 MOE_TIC(t_w);
-                const bool ok0 = ring_wait(&full[s0], (ci / S) & 1, abort, hdr, (uint32_t)ci);
-                const bool ok1 =
-                    ring_wait(&full[s1], ((ci + 1) / S) & 1, abort, hdr, (uint32_t)ci + 1);
+                const bool ok0 = ring_wait(&full[s0], p0, abort, hdr, (uint32_t)ci);
+                const bool ok1 = ring_wait(&full[s1], p1, abort, hdr, (uint32_t)ci + 1);
                 MOE_TOC(tid == 0, 18, t_w);
                 MOE_TIC(t_c);
                 const uint8_t *sg = ring + (size_t)s0 * p.slot_bytes;
@@ -646,68 +658,75 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         named_bar(2, kComputeAndEpi);
         MOE_PHASE_MARK(tid == 0, 7);
 
-        // phase D: down, 32 output rows per unit (two MMA tiles, four chains)
+        // phase D: down, 32 output rows per unit (two MMA tiles, four chains).
+        // The units of one entry run in an inner loop that only waits,
+        // multiplies and hands the partial sums over; the entry's h
+        // fragments are loaded once before it.
         {
             uint32_t bh[MC_D][8][2];
             float inv0 = 1.f, inv1 = 1.f;
-            int cur = -1;
-            for (int j = d_begin; j < d_end; ++j) {
-                int entry, K;
+            int j = d_begin;
+            while (j < d_end) {
+                int entry, K, jend;
                 uint32_t mask;
                 if (j < Sd) {
                     entry = kSharedEntry;
                     K = p.Is;
                     mask = allrows;
+                    jend = min(Sd, d_end);
                 } else {
                     entry = (j - Sd) / Ho;
                     K = p.I;
                     mask = sm.uni.rowmask[entry];
+                    jend = min(Sd + (entry + 1) * Ho, d_end);
                 }
                 const int nch = K / kChunk;
+                const uint32_t rowb = (uint32_t)K / 2, scb = (uint32_t)K / 16;
                 MOE_TIC(t_b);
-                if (entry != cur) {
-                    load_b<MC_D>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
-                                 (size_t)p.ws.inter_max, mask, nch, warp, kConsumerWarps, lane,
-                                 bh, inv0, inv1);
-                    cur = entry;
-                }
+                load_b<MC_D>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
+                             (size_t)p.ws.inter_max, mask, nch, warp, kConsumerWarps, lane, bh,
+                             inv0, inv1);
                 MOE_TOC(tid == 0, 21, t_b);
-                MOE_TIC(t_dw);
-                const int s = ci % S;
-                const bool ok = ring_wait(&full[s], (ci / S) & 1, abort, hdr, (uint32_t)ci);
-                MOE_TOC(tid == 0, 22, t_dw);
-                MOE_TIC(t_dc);
-                const uint8_t *st = ring + (size_t)s * p.slot_bytes;
-                const uint8_t *sc = st + kOutTile * K / 2;
-                float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-                float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                if (ok) {
+                for (; j < jend; ++j) {
+                    const int s = rs;
+                    const uint32_t par = rp;
+                    next_slot();
+                    MOE_TIC(t_dw);
+                    const bool ok = ring_wait(&full[s], par, abort, hdr, (uint32_t)ci);
+                    MOE_TOC(tid == 0, 22, t_dw);
+                    MOE_TIC(t_dc);
+                    const uint8_t *st = ring + (size_t)s * p.slot_bytes;
+                    const uint8_t *sc = st + kOutTile * rowb;
+                    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+                    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                    if (ok) {
 #pragma unroll
-                    for (int m = 0; m < MC_D; ++m) {
-                        const int c = warp + kConsumerWarps * m;
-                        if (c < nch) {
-                            chunk_mma(st, sc, K / 2, K / 16, c, g, q, bh[m], a0, a1);
-                            chunk_mma(st + kTileRows * (K / 2), sc + kTileRows * (K / 16), K / 2,
-                                      K / 16, c, g, q, bh[m], c0, c1);
+                        for (int m = 0; m < MC_D; ++m) {
+                            const int c = warp + kConsumerWarps * m;
+                            if (c < nch) {
+                                chunk_mma(st, sc, rowb, scb, c, g, q, bh[m], a0, a1);
+                                chunk_mma(st + kTileRows * rowb, sc + kTileRows * scb, rowb, scb, c,
+                                          g, q, bh[m], c0, c1);
+                            }
                         }
                     }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-                ++ci;
-                float da[4], dc[4];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s]);
+                    ++ci;
+                    float da[4], dc[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    da[i] = a0[i] + a1[i];
-                    dc[i] = c0[i] + c1[i];
+                    for (int i = 0; i < 4; ++i) {
+                        da[i] = a0[i] + a1[i];
+                        dc[i] = c0[i] + c1[i];
+                    }
+                    MOE_TOC(tid == 0, 23, t_dc);
+                    const int rb = claim_red();
+                    store_partial(sm.red[rb][warp], da, g, q, inv0, inv1);
+                    store_partial(sm.red[rb][warp] + 128, dc, g, q, inv0, inv1);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.red_full[rb]);
+                    ++ui;
                 }
-                MOE_TOC(tid == 0, 23, t_dc);
-                const int rb = claim_red();
-                store_partial(sm.red[rb][warp], da, g, q, inv0, inv1);
-                store_partial(sm.red[rb][warp] + 128, dc, g, q, inv0, inv1);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.red_full[rb]);
-                ++ui;
             }
         }
         MOE_PHASE_MARK(tid == 0, 8);
