@@ -7,6 +7,7 @@ import torch
 
 from oracle import oracle
 from routed_moe_decode_router_gb300 import layer as L
+from routed_moe_decode_router_gb300 import native as N
 from routed_moe_decode_router_gb300 import synth
 from tests import gpu_util as G
 
@@ -145,6 +146,27 @@ def test_device_status_on_bad_expert_id():
     assert ws.status() == 0          # cleared by the read
     torch.zeros(1, device="cuda").add_(1)
     torch.cuda.synchronize()
+
+
+def test_grid_barrier_timeout_sets_status_and_context_survives():
+    """A bounded wait that runs out records MOE_DEV_WAIT_TIMEOUT and the
+    context stays usable.  The workspace's grid-barrier counter (header offset
+    16) is skewed to G - 1, so the first CTA at barrier 1 completes it and the
+    other G - 1 wait for arrivals that never come; their waits run out after
+    about two seconds, they skip the rest of the layer, and the launch ends."""
+    weights, x = G.make_case(TINY, 2, seed_w=31, seed_x=32)
+    ws = L.Workspace(TINY)
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    ws.buf[16:24].view(torch.int64).fill_(grid - 1)
+    dl = L.DeviceLayer(weights)
+    L.forward(dl, x, ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 3          # MOE_DEV_WAIT_TIMEOUT
+    assert ws.status() == 0          # cleared by the read
+    # a fresh header, and the same workspace computes the layer again
+    N.moe_workspace_init(ws.ptr, ws.nbytes, 0)
+    res = G.gpu_run(weights, x, ws=ws, dl=dl)
+    G.check_parity(weights, x, res)
 
 
 def test_workspace_reuse_across_row_counts():
