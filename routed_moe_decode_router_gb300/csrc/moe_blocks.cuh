@@ -464,6 +464,7 @@ __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, volati
             record_fault(hdr, MOE_DEV_WAIT_TIMEOUT, info);
             return false;
         }
+        __nanosleep(64);   // leave issue slots to the warps that share the sub-partition
     }
     return true;
 }
