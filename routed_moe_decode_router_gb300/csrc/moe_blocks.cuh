@@ -172,6 +172,22 @@ __device__ __forceinline__ void warp_topk_row_nk(const float *lg, const float *b
     }
 }
 
+// The same with the candidate count fixed at compile time (TK = the class of
+// E: 0 for E <= 128, 1 for <= 256, 2 for <= 512, 3 for <= 1024).
+template <int TK>
+__device__ __forceinline__ void warp_topk_row_tk(const float *lg, const float *bias, int E, int k,
+                                                 int scoring, int norm, float rsf,
+                                                 int32_t *ids_out, float *wts_out, int lane) {
+    if constexpr (TK == 0)
+        warp_topk_row_nk<4, 1>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+    else if constexpr (TK == 1)
+        warp_topk_row_nk<8, 1>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+    else if constexpr (TK == 2)
+        warp_topk_row_nk<16, 1>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+    else
+        warp_topk_row_nk<16, 2>(lg, bias, E, k, scoring, norm, rsf, ids_out, wts_out, lane);
+}
+
 __device__ __forceinline__ void warp_topk_row(const float *lg, const float *bias, int E, int k,
                                               int scoring, int norm, float rsf, int32_t *ids_out,
                                               float *wts_out, int lane) {

@@ -1,806 +1,54 @@
-// moe_layer.cu -- the whole routed MoE layer as one persistent kernel.
-//
-// One CTA per SM (every CTA resident at once): 8 compute warps, 2 epilogue
-// warps (cross-warp reductions and output stores; they take alternate units,
-// each fed through its own buffer of partial sums behind mbarriers, so the
-// compute warps rarely wait for an epilogue) and 1 producer warp (bulk
-// copies).  Phases:
-//   A  router: the E router rows (plus the shared-expert gate vector as row
-//      E) are spread over the CTAs; each row's dot products for all token
-//      rows are split over the compute warps (forward_token_major.rs:
-//      dense_gemm / w4a16_gemm).  Meanwhile the producer stages this CTA's
-//      first shared-expert gate/up tiles, which need no routing.
-//   -  grid barrier (all logits written)
-//   B  every CTA computes the top-k of every row and the union itself, from
-//      the logits in L2 -- the same result in every CTA, so no second
-//      exchange is needed (page "Function forward_moe", RETRACTED and WIDENED
-//      notes: rows * top_k <= 64 ids in one block by pairwise scan, no sort,
-//      nothing sent to the host); the producer then fetches the union
-//      experts' pointer entries.
-//   C  gate+up sweep: units = 16-row tiles of an entry's gate and up
-//      matrices (shared expert first, then the union experts), CTA b takes
-//      units b, b + G, ...; h = bf16(silu(g) * v) to the workspace
-//      (moe_expert_gate_up_shared_prefill).
-//   -  grid barrier (every h written); the producer keeps streaming down
-//      tiles through it
-//   D  down sweep: units = 32-row tiles of an entry's down matrix, CTA b
-//      takes a contiguous range (h fragments stay in registers per entry);
-//      y (fp32) per (row, slot) to the workspace
-//      (moe_expert_silu_down_shared_prefill).
-//   -  grid barrier (every y written)
-//   E  blend, spread over the CTAs by (32-row output tile, token row):
-//        out[r][o] = bf16( sum_{slot<k} w[r][slot] * y[r][slot][o] + g_r * ys[r][o] )
-//      in slot order (moe_weighted_sum_blend_prefill).
-//
-// Weight tiles (contiguous 16 x K/2 packed + 16 x K/16 scale bytes) move by
-// bulk (TMA) copies into a ring of shared-memory slots behind mbarriers with
-// an evict-first L2 policy; gate and up of one unit occupy two slots, a down
-// unit one.  The MMA is mma.sync m16n8k16 (f16 x f16 -> fp32) with the NVFP4
-// weights unpacked to f16 in registers and the token rows as the 8 columns.
-//
-// Every wait is bounded (ring waits, the three grid barriers); a wait that
-// runs out records MOE_DEV_WAIT_TIMEOUT, and the CTA skips the rest of its
-// work.
+// moe_layer.cu -- host side of the layer kernel: shared-memory sizing,
+// kernel selection (MC_GU, MC_D, top-k class) and the cooperative, PDL launch.
+// The kernel itself is in moe_layer_kernel.cuh, instantiated in
+// moe_layer_tk0.cu .. moe_layer_tk3.cu.
 #include <cuda_runtime.h>
 
-#include "moe_blocks.cuh"
-
-// Phase marks and cycle accumulators: no-ops unless the library is built with
-// MOE_TRACE, which must then provide moe_trace_mark(cta, mark) (a per-CTA
-// timestamp store) and moe_trace_add(cta, slot, cycles).
-#ifdef MOE_TRACE
-__device__ void moe_trace_mark(int cta, int mark);
-__device__ void moe_trace_add(int cta, int slot, long long cycles);
-#define MOE_PHASE_MARK(cond, i) \
-    do {                        \
-        if (cond) moe_trace_mark(blockIdx.x, (i)); \
-    } while (0)
-#define MOE_TIC(v) const long long v = clock64()
-#define MOE_TOC(cond, i, v) \
-    do {                    \
-        if (cond) moe_trace_add(blockIdx.x, (i), clock64() - (v)); \
-    } while (0)
-#else
-#define MOE_PHASE_MARK(cond, i) \
-    do {                        \
-    } while (0)
-#define MOE_TIC(v) \
-    do {           \
-    } while (0)
-#define MOE_TOC(cond, i, v) \
-    do {                    \
-    } while (0)
-#endif
+#include "moe_layout.h"
 
 namespace moe {
 
-constexpr int kRouterRowsPerPass = 4;     // router rows of one CTA handled together
-constexpr int kMaxSegs = MOE_MAX_HIDDEN / 256;
-constexpr int kRed = 2;                   // partial-sum buffers between compute and epilogue
-constexpr int kEpiWarp = kConsumerWarps;        // warp 8: first epilogue warp (and the union)
-constexpr int kProdWarp = kConsumerWarps + 1;   // warp 9: bulk-copy producer
-constexpr int kEpiWarp2 = kConsumerWarps + 2;   // warp 10: second epilogue warp
-constexpr int kEpiWarps = 2;                    // epilogue warp e takes units ui with ui % 2 == e
-constexpr int kLayerThreads = (kConsumerWarps + 3) * 32;
-constexpr int kComputeAndEpi = (kConsumerWarps + kEpiWarps) * 32;
-static_assert(kRed == kEpiWarps, "each epilogue warp owns one partial-sum buffer");
-
-struct LayerSmem {
-    float red[kRed][kConsumerWarps][256];       // compute warps' partial sums
-    float rpart[kRouterRowsPerPass][kMaxSegs][kMaxRows];   // router partial dots
-    moe_union_table uni;
-    PtrEntry ptrs[kEntries];
-    int32_t ids[kMaxIds];
-    float wts[kMaxIds];
-    float gate_val[kMaxRows];
-    uint32_t umask[kMaxIds];
-    uint64_t red_full[kRed];                    // partials ready (8 compute-warp arrivals)
-    uint64_t red_empty[kRed];                   // partials consumed (1 epilogue arrival)
-    int abort;
-};
-
-constexpr size_t kLayerSmemFixed = (sizeof(LayerSmem) + 127) & ~size_t(127);
+void *layer_kernel_tk0(int mc_gu, int mc_d);
+void *layer_kernel_tk1(int mc_gu, int mc_d);
+void *layer_kernel_tk2(int mc_gu, int mc_d);
+void *layer_kernel_tk3(int mc_gu, int mc_d);
+size_t layer_fixed_smem_bytes();
 
 size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
-    return kLayerSmemFixed + (size_t)stages * slot_bytes + 2 * sizeof(uint64_t) * stages;
+    return layer_fixed_smem_bytes() + (size_t)stages * slot_bytes + 2 * sizeof(uint64_t) * stages;
 }
 
-// Raw router weights of row `row` (E = the shared-expert gate vector) at the
-// 8 inputs h0..h0+7: a uint4 of bf16 values, or (NVFP4) the packed word in
-// .x and the E4M3 scale byte in .y.  Loads only, so that several rows' loads
-// can be in flight before any is used.
-__device__ __forceinline__ uint4 router_raw(const LayerParams &p, int row, int h0) {
-    const int H = p.H;
-    if (row == p.E || p.router_fmt == MOE_ROUTER_BF16) {
-        const uint16_t *src = (row == p.E) ? p.sh_vec + h0 : p.router_bf16 + (size_t)row * H + h0;
-        return ld_nc_v4(src);
+// Top-k class of a router width (the top-k keeps E / 32 candidates per lane
+// in registers: 4, 8, 16 or two lists of 16).
+static int topk_class(int E) { return E <= 128 ? 0 : (E <= 256 ? 1 : (E <= 512 ? 2 : 3)); }
+
+static void *layer_kernel(int mc_gu, int mc_d, int tk) {
+    switch (tk) {
+    case 0: return layer_kernel_tk0(mc_gu, mc_d);
+    case 1: return layer_kernel_tk1(mc_gu, mc_d);
+    case 2: return layer_kernel_tk2(mc_gu, mc_d);
+    default: return layer_kernel_tk3(mc_gu, mc_d);
     }
-    uint4 r;
-    r.x = *reinterpret_cast<const uint32_t *>(p.router_fp4.packed + (size_t)row * (H / 2) + h0 / 2);
-    r.y = p.router_fp4.scales[(size_t)row * (H / 16) + h0 / 16];
-    r.z = r.w = 0u;
-    return r;
-}
-
-// The 8 weights of router_raw as fp32 (NVFP4: e2m1 * e4m3; scale2 comes later).
-__device__ __forceinline__ void router_decode(const LayerParams &p, int row, uint4 v, float (&w)[8]) {
-    if (row == p.E || p.router_fmt == MOE_ROUTER_BF16) {
-        w[0] = bf16_lo(v.x); w[1] = bf16_hi(v.x); w[2] = bf16_lo(v.y); w[3] = bf16_hi(v.y);
-        w[4] = bf16_lo(v.z); w[5] = bf16_hi(v.z); w[6] = bf16_lo(v.w); w[7] = bf16_hi(v.w);
-    } else {
-        const uint32_t sh = e4m3x2_to_f16x2(v.y);
-        const float sc = __low2float(*reinterpret_cast<const __half2 *>(&sh));
-        uint32_t hq[4];
-        e2m1x8_to_f16x2(v.x, hq);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __half2 qv = *reinterpret_cast<const __half2 *>(&hq[i]);
-            w[2 * i] = __low2float(qv) * sc;
-            w[2 * i + 1] = __high2float(qv) * sc;
-        }
-    }
-}
-
-template <int MC_GU, int MC_D>
-__global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const LayerParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    LayerSmem &sm = *reinterpret_cast<LayerSmem *>(smem);
-    uint8_t *ring = smem + kLayerSmemFixed;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring + (size_t)p.stages * p.slot_bytes);
-    uint64_t *empty = full + p.stages;
-    volatile int *abort = &sm.abort;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = gridDim.x, b = blockIdx.x, S = p.stages;
-    const int H = p.H, E = p.E, k = p.k;
-    const int It = p.I / kTileRows;
-    const int St = p.has_shared ? p.Is / kTileRows : 0;
-    const int Ho = H / kOutTile;                 // down units (32 rows) per entry
-    const int Sd = p.has_shared ? Ho : 0;
-    const bool is_comp = warp < kConsumerWarps;
-    const bool is_epi = warp == kEpiWarp || warp == kEpiWarp2;
-    const int epi_idx = warp == kEpiWarp2 ? 1 : 0;
-    const bool is_prod = warp == kProdWarp;
-    const bool gate_row = p.has_shared && p.shared_gated;
-    const int nrow = E + (gate_row ? 1 : 0);
-    const uint32_t gu_pk = kTileRows * H / 2, gu_sc = kTileRows * H / 16;
-    WsHeader *hdr = p.ws.hdr;
-
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
-        }
-        for (int r = 0; r < kRed; ++r) {
-            mbar_init(&sm.red_full[r], kConsumerWarps);
-            mbar_init(&sm.red_empty[r], 1);
-        }
-        fence_mbar_init();
-        sm.abort = 0;
-    }
-    __syncthreads();
-    MOE_PHASE_MARK(tid == 0, 0);
-
-    // ---------------- producer: slot issue helpers (lane 0 only) ----------------
-    uint64_t pol = 0;
-    int pi = 0;   // slots issued
-    auto acquire = [&](int i) -> bool {
-        if (i < S) return !*abort;
-        return ring_wait(&empty[i % S], ((i / S) - 1) & 1, abort, hdr, 0x100000u + (uint32_t)i);
-    };
-    auto issue_pair = [&](const uint8_t *pk, const uint8_t *sc, uint32_t pkb, uint32_t scb) {
-        const int s = pi % S;
-        uint8_t *st = ring + (size_t)s * p.slot_bytes;
-        mbar_arrive_expect_tx(&full[s], pkb + scb);
-        bulk_g2s(st, pk, pkb, &full[s], pol);
-        bulk_g2s(st + pkb, sc, scb, &full[s], pol);
-        ++pi;
-    };
-    auto issue_empty = [&]() -> bool {
-        if (!acquire(pi)) return false;
-        mbar_arrive(&full[pi % S]);
-        ++pi;
-        return true;
-    };
-    // gate+up unit j (16 rows): a gate slot, then an up slot
-    auto issue_gu = [&](int j) -> bool {
-        const uint8_t *gp, *gs, *upk, *us;
-        if (j < St) {
-            gp = p.sh_gate.packed + (size_t)j * gu_pk;
-            gs = p.sh_gate.scales + (size_t)j * gu_sc;
-            upk = p.sh_up.packed + (size_t)j * gu_pk;
-            us = p.sh_up.scales + (size_t)j * gu_sc;
-        } else {
-            const PtrEntry &e = sm.ptrs[(j - St) / It];
-            const int tile = (j - St) % It;
-            if (e.expert < 0) return issue_empty() && issue_empty();
-            gp = e.packed[0] + (size_t)tile * gu_pk;
-            gs = e.scales[0] + (size_t)tile * gu_sc;
-            upk = e.packed[1] + (size_t)tile * gu_pk;
-            us = e.scales[1] + (size_t)tile * gu_sc;
-        }
-        if (!acquire(pi)) return false;
-        issue_pair(gp, gs, gu_pk, gu_sc);
-        if (!acquire(pi)) return false;
-        issue_pair(upk, us, gu_pk, gu_sc);
-        return true;
-    };
-
-    int pj = b;   // next gate+up unit of this CTA
-    if (is_prod && lane == 0) {
-        pol = l2_evict_first_policy();
-        while (pj < St && pi + 2 <= S) {
-            issue_gu(pj);
-            pj += G;
-        }
-        MOE_PHASE_MARK(true, 11);
-    }
-    // L2 prefetch of this CTA's router rows and of the expert tables
-    if (is_comp && lane == 0) {
-        for (int row = b + G * warp; row < nrow; row += G * kConsumerWarps) {
-            const void *src;
-            uint32_t bytes;
-            if (row == E) {
-                src = p.sh_vec;
-                bytes = H * 2;
-            } else if (p.router_fmt == MOE_ROUTER_BF16) {
-                src = p.router_bf16 + (size_t)row * H;
-                bytes = H * 2;
-            } else {
-                src = p.router_fp4.packed + (size_t)row * (H / 2);
-                bytes = H / 2;
-            }
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes)
-                         : "memory");
-        }
-    }
-    if (b < 3 && warp == 0) {
-        const moe_expert_table &t = b == 0 ? p.gate : (b == 1 ? p.up : p.down);
-        for (int off = lane * 128; off < E * 8; off += 32 * 128) {
-            asm volatile("prefetch.global.L2 [%0];" ::"l"((const char *)t.packed + off));
-            asm volatile("prefetch.global.L2 [%0];" ::"l"((const char *)t.scales + off));
-        }
-        for (int off = lane * 128; off < E * 4; off += 32 * 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"((const char *)t.scale2 + off));
-    }
-    pdl_trigger();
-    pdl_wait();
-    MOE_PHASE_MARK(tid == 0, 1);
-
-    // ---------------- phase A: router rows ----------------
-    // This CTA's rows are b, b + G, ... (at most kRouterRowsPerPass per
-    // pass).  Compute warp w takes the 256-input segments w, w + 8, ...: it
-    // loads the token rows' inputs of its segment once, then the weights of
-    // every row of the pass, all before the first use, so one memory latency
-    // covers the pass.  Partial sums are added in segment order.
-    if (is_comp) {
-        const int my_rows = b < nrow ? (nrow - b + G - 1) / G : 0;
-        const int nseg = (H + 255) / 256;
-        for (int r0 = 0; r0 < my_rows; r0 += kRouterRowsPerPass) {
-            const int nr = min(kRouterRowsPerPass, my_rows - r0);
-            for (int seg = warp; seg < nseg; seg += kConsumerWarps) {
-                const int h0 = seg * 256 + lane * 8;
-                const bool live = h0 < H;   // H is a multiple of 128, not always of 256
-                const int hc = live ? h0 : 0;
-                // every load first, from clamped addresses; unused values are zeroed after
-                uint4 xv[kMaxRows];
-#pragma unroll
-                for (int r = 0; r < kMaxRows; ++r)
-                    if (r < p.rows) xv[r] = ld_cg_v4(p.x + (size_t)r * H + hc);
-                uint4 rv[kRouterRowsPerPass];
-#pragma unroll
-                for (int ri = 0; ri < kRouterRowsPerPass; ++ri)
-                    rv[ri] = router_raw(p, b + (r0 + min(ri, nr - 1)) * G, hc);
-#pragma unroll
-                for (int r = 0; r < kMaxRows; ++r)
-                    if (!live || r >= p.rows) xv[r] = make_uint4(0u, 0u, 0u, 0u);
-                float wv[kRouterRowsPerPass][8];
-#pragma unroll
-                for (int ri = 0; ri < kRouterRowsPerPass; ++ri) {
-                    router_decode(p, b + (r0 + min(ri, nr - 1)) * G, rv[ri], wv[ri]);
-                    if (!live || ri >= nr) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) wv[ri][i] = 0.f;
-                    }
-                }
-#pragma unroll
-                for (int ri = 0; ri < kRouterRowsPerPass; ++ri) {
-                    if (ri >= nr) break;
-#pragma unroll
-                    for (int r = 0; r < kMaxRows; ++r) {
-                        if (r >= p.rows) break;
-                        const uint4 x4 = xv[r];
-                        float a = 0.f;
-                        a = fmaf(bf16_lo(x4.x), wv[ri][0], a);
-                        a = fmaf(bf16_hi(x4.x), wv[ri][1], a);
-                        a = fmaf(bf16_lo(x4.y), wv[ri][2], a);
-                        a = fmaf(bf16_hi(x4.y), wv[ri][3], a);
-                        a = fmaf(bf16_lo(x4.z), wv[ri][4], a);
-                        a = fmaf(bf16_hi(x4.z), wv[ri][5], a);
-                        a = fmaf(bf16_lo(x4.w), wv[ri][6], a);
-                        a = fmaf(bf16_hi(x4.w), wv[ri][7], a);
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                        if (lane == 0) sm.rpart[ri][seg][r] = a;
-                    }
-                }
-            }
-            named_bar(1, kConsumerWarps * 32);
-            for (int t = tid; t < nr * p.rows; t += kConsumerWarps * 32) {
-                const int ri = t / p.rows, r = t % p.rows;
-                const int row = b + (r0 + ri) * G;
-                float v = 0.f;
-                for (int seg = 0; seg < nseg; ++seg) v += sm.rpart[ri][seg][r];
-                if (row == E) {
-                    p.ws.gate_val[r] = 1.f / (1.f + expf(-v));
-                } else {
-                    if (p.router_fmt == MOE_ROUTER_NVFP4) v *= p.router_fp4.scale2;
-                    p.ws.logits[(size_t)r * E + row] = v;
-                }
-            }
-            named_bar(1, kConsumerWarps * 32);
-        }
-    }
-    __syncthreads();
-    MOE_PHASE_MARK(tid == 0, 2);
-    if (tid == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 1u);
-    __syncthreads();
-    MOE_PHASE_MARK(tid == 0, 3);
-
-    // ---------------- phase B: top-k and union, in every CTA ----------------
-    // One warp per token row selects its experts; then the epilogue warp
-    // builds the union and the union experts' pointer entries while the
-    // compute warps load their token-row fragments, and publishes both
-    // through named barrier 4.
-    if (warp == kEpiWarp && lane < kMaxRows)
-        sm.gate_val[lane] = !p.has_shared ? 0.f : (gate_row ? ld_cg(p.ws.gate_val + lane) : 1.f);
-    MOE_TIC(t_topk);
-    if (warp < p.rows)
-        warp_topk_row(p.ws.logits + (size_t)warp * E, p.bias, E, k, p.scoring, p.norm, p.rsf,
-                      sm.ids + warp * k, sm.wts + warp * k, lane);
-    MOE_TOC(tid == 0, 16, t_topk);
-    __syncthreads();
-    if (warp == kEpiWarp) {
-        MOE_TIC(t_union);
-        UnionSrc src{E,      k,      p.rows, p.per_row_mode, 1,        p.has_shared,
-                     p.gate, p.up,   p.down, p.sh_gate,      p.sh_up, p.sh_down};
-        build_union(src, sm.ids, sm.umask, &sm.uni, sm.ptrs, hdr, lane);
-        __syncwarp();
-        asm volatile("bar.arrive 4, %0;" ::"r"(kLayerThreads) : "memory");
-        MOE_TOC(lane == 0, 17, t_union);
-        MOE_PHASE_MARK(lane == 0, 4);
-        if (b == 0) {   // publish the routing for moe_read_routing
-            const int n = p.rows * k;
-            for (int i = lane; i < n; i += 32) {
-                p.ws.ids[i] = sm.ids[i];
-                p.ws.wts[i] = sm.wts[i];
-            }
-            const uint32_t *su = reinterpret_cast<const uint32_t *>(&sm.uni);
-            uint32_t *du = reinterpret_cast<uint32_t *>(p.ws.uni);
-            for (int i = lane; i < (int)(sizeof(moe_union_table) / 4); i += 32) du[i] = su[i];
-            if (lane < kMaxRows && !gate_row) p.ws.gate_val[lane] = sm.gate_val[lane];
-        }
-    } else if (is_prod || warp == kEpiWarp2) {
-        named_bar(4, kLayerThreads);
-    }
-    // (the compute warps pass barrier 4 after loading their fragments)
-    const uint32_t allrows = (1u << p.rows) - 1u;
-    int U = 0, Tgu = 0, Td = 0, d_begin = 0, d_end = 0;
-    auto sweep_layout = [&]() {
-        U = sm.uni.num_union;
-        Tgu = St + U * It;
-        Td = Sd + U * Ho;
-        d_begin = (int)((long long)b * Td / G);
-        d_end = (int)((long long)(b + 1) * Td / G);
-    };
-
-    // ---------------- producer: pointer table, then every remaining slot ----------------
-    if (is_prod) {
-        sweep_layout();
-        if (lane == 0) {
-            bool ok = true;
-            for (; ok && pj < Tgu; pj += G) ok = issue_gu(pj);
-            for (int j = d_begin; ok && j < d_end; ++j) {
-                const uint8_t *dp, *ds;
-                int K;
-                if (j < Sd) {
-                    K = p.Is;
-                    dp = p.sh_down.packed + (size_t)j * kOutTile * (K / 2);
-                    ds = p.sh_down.scales + (size_t)j * kOutTile * (K / 16);
-                } else {
-                    const PtrEntry &e = sm.ptrs[(j - Sd) / Ho];
-                    const int tile = (j - Sd) % Ho;
-                    if (e.expert < 0) {
-                        ok = issue_empty();
-                        continue;
-                    }
-                    K = p.I;
-                    dp = e.packed[2] + (size_t)tile * kOutTile * (K / 2);
-                    ds = e.scales[2] + (size_t)tile * kOutTile * (K / 16);
-                }
-                if (!(ok = acquire(pi))) break;
-                issue_pair(dp, ds, kOutTile * K / 2, kOutTile * K / 16);
-            }
-            MOE_PHASE_MARK(true, 10);
-        }
-        return;
-    }
-
-    if (is_epi) {
-        // ---------------- epilogue warp ----------------
-        // Everything a unit's epilogue needs except the partial sums (entry,
-        // tile, scales, row mask, destination) is fetched before waiting for
-        // them, and the eight warps' partials are loaded unconditionally and
-        // summed with a select, so one shared-memory latency covers them.
-        sweep_layout();
-        int ui = 0;
-        const int nwg = min(kConsumerWarps, H / kChunk);   // warps holding gate/up partials
-        const int col = lane >> 2, rq = lane & 3;
-        for (int j = b; j < Tgu; j += G, ++ui) {
-            if ((ui & 1) != epi_idx) continue;
-            const int rb = ui % kRed;
-            int entry, tile;
-            float s2g, s2u;
-            uint32_t mask;
-            bool live = true;
-            if (j < St) {
-                entry = kSharedEntry;
-                tile = j;
-                s2g = p.sh_gate.scale2;
-                s2u = p.sh_up.scale2;
-                mask = allrows;
-            } else {
-                entry = (j - St) / It;
-                tile = (j - St) % It;
-                live = sm.ptrs[entry].expert >= 0;
-                s2g = sm.ptrs[entry].scale2[0];
-                s2u = sm.ptrs[entry].scale2[1];
-                mask = sm.uni.rowmask[entry];
-            }
-            live = live && ((mask >> col) & 1u);
-            // lane: column col, rows 4 * rq .. + 3 of the 16-row tile
-            const int off = partial_index(col, 4 * rq);
-            MOE_TIC(t_ew);
-            ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
-            MOE_TOC(lane == 0, 25, t_ew);
-            MOE_TIC(t_ex);
-            float4 ga[kConsumerWarps], ua[kConsumerWarps];
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                ga[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][off]);
-                ua[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][128 + off]);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.red_empty[rb]);   // the values are in registers
-            float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const bool on = w < nwg;
-                gs[0] += on ? ga[w].x : 0.f; gs[1] += on ? ga[w].y : 0.f;
-                gs[2] += on ? ga[w].z : 0.f; gs[3] += on ? ga[w].w : 0.f;
-                us[0] += on ? ua[w].x : 0.f; us[1] += on ? ua[w].y : 0.f;
-                us[2] += on ? ua[w].z : 0.f; us[3] += on ? ua[w].w : 0.f;
-            }
-            if (live && !*abort) {
-                uint32_t hv[2];
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    float h2[2];
-#pragma unroll
-                    for (int z = 0; z < 2; ++z) {
-                        const float gv = gs[2 * i + z] * s2g, uv = us[2 * i + z] * s2u;
-                        h2[z] = silu(gv) * uv;
-                    }
-                    hv[i] = (uint32_t)f2bf16_rn(h2[0]) | ((uint32_t)f2bf16_rn(h2[1]) << 16);
-                }
-                *reinterpret_cast<uint2 *>(p.ws.hbuf +
-                                           ((size_t)entry * kMaxRows + col) * p.ws.inter_max +
-                                           tile * kTileRows + 4 * rq) = make_uint2(hv[0], hv[1]);
-            }
-            MOE_TOC(lane == 0, 26, t_ex);
-        }
-        // every h of this CTA is stored (both epilogue warps): grid barrier,
-        // then release the compute warps
-        named_bar(5, kEpiWarps * 32);
-        MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 13);
-        if (lane == 0 && epi_idx == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 2u);
-        named_bar(5, kEpiWarps * 32);
-        MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 14);
-        asm volatile("bar.arrive 2, %0;" ::"r"(kComputeAndEpi) : "memory");
-        // lane: column col, rows 8 * (rq & 1) .. + 7 of MMA tile rq >> 1
-        const int half = rq >> 1, r0 = (rq & 1) * 8;
-        for (int j = d_begin; j < d_end; ++j, ++ui) {
-            if ((ui & 1) != epi_idx) continue;
-            const int rb = ui % kRed;
-            int entry, tile, K;
-            uint32_t mask;
-            float s2;
-            bool live = true;
-            if (j < Sd) {
-                entry = kSharedEntry;
-                tile = j;
-                K = p.Is;
-                mask = allrows;
-                s2 = p.sh_down.scale2;
-            } else {
-                entry = (j - Sd) / Ho;
-                tile = (j - Sd) % Ho;
-                K = p.I;
-                mask = sm.uni.rowmask[entry];
-                live = sm.ptrs[entry].expert >= 0;
-                s2 = sm.ptrs[entry].scale2[2];
-            }
-            live = live && ((mask >> col) & 1u);
-            const int nwd = min(kConsumerWarps, K / kChunk);   // warps holding down partials
-            const int o = tile * kOutTile + half * kTileRows + r0;
-            float *dst = (entry == kSharedEntry)
-                             ? p.ws.ysbuf + (size_t)col * H + o
-                             : p.ws.ybuf + ((size_t)col * k + (live ? sm.uni.uslot[entry][col] : 0)) * H + o;
-            const int off0 = half * 128 + partial_index(col, r0);
-            const int off1 = half * 128 + partial_index(col, r0 + 4);
-            MOE_TIC(t_ew);
-            ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
-            MOE_TOC(lane == 0, 27, t_ew);
-            MOE_TIC(t_ex);
-            float4 a[kConsumerWarps], c[kConsumerWarps];
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                a[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][off0]);
-                c[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][off1]);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.red_empty[rb]);
-            float ys[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const bool on = w < nwd;
-                ys[0] += on ? a[w].x : 0.f; ys[1] += on ? a[w].y : 0.f;
-                ys[2] += on ? a[w].z : 0.f; ys[3] += on ? a[w].w : 0.f;
-                ys[4] += on ? c[w].x : 0.f; ys[5] += on ? c[w].y : 0.f;
-                ys[6] += on ? c[w].z : 0.f; ys[7] += on ? c[w].w : 0.f;
-            }
-            if (live && !*abort) {
-                *reinterpret_cast<float4 *>(dst) =
-                    make_float4(ys[0] * s2, ys[1] * s2, ys[2] * s2, ys[3] * s2);
-                *reinterpret_cast<float4 *>(dst + 4) =
-                    make_float4(ys[4] * s2, ys[5] * s2, ys[6] * s2, ys[7] * s2);
-            }
-            MOE_TOC(lane == 0, 28, t_ex);
-        }
-        named_bar(5, kEpiWarps * 32);
-        MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 15);
-        if (lane == 0 && epi_idx == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 3u);
-        named_bar(5, kEpiWarps * 32);   // both epilogue warps read y in the blend
-        asm volatile("bar.arrive 3, %0;" ::"r"(kComputeAndEpi) : "memory");
-    } else {
-        // ---------------- compute warps ----------------
-        const int g = lane >> 2, q = lane & 3;
-        int ci = 0;          // slots consumed
-        int rs = 0;          // ring slot of the next tile, and its phase parity
-        uint32_t rp = 0u;
-        auto next_slot = [&]() {
-            if (++rs == S) {
-                rs = 0;
-                rp ^= 1u;
-            }
-        };
-        int ui = 0;   // units handed to the epilogue warps
-        // wait until the epilogue warp has consumed the buffer this unit reuses
-        auto claim_red = [&]() -> int {
-            const int rb = ui % kRed;
-            MOE_TIC(t_rw);
-            if (ui >= kRed)
-                ring_wait(&sm.red_empty[rb], ((ui / kRed) - 1) & 1, abort, hdr,
-                          0x300000u + (uint32_t)ui);
-            MOE_TOC(tid == 0, 20, t_rw);
-            return rb;
-        };
-
-        // phase C: gate + up (both slots of a unit, the two matrices interleaved)
-        {
-            uint32_t bx[MC_GU][8][2];
-            float inv0, inv1;
-            load_b<MC_GU>(p.x, (size_t)H, allrows, H / kChunk, warp, kConsumerWarps, lane, bx,
-                          inv0, inv1);
-            MOE_PHASE_MARK(tid == 0, 5);
-            named_bar(4, kLayerThreads);
-            sweep_layout();
-            const int nch = H / kChunk;
-            for (int j = b; j < Tgu; j += G) {
-                const int s0 = rs;
-                const uint32_t p0 = rp;
-                next_slot();
-                const int s1 = rs;
-                const uint32_t p1 = rp;
-                next_slot();
-                MOE_TIC(t_w);
-                const bool ok0 = ring_wait(&full[s0], p0, abort, hdr, (uint32_t)ci);
-                const bool ok1 = ring_wait(&full[s1], p1, abort, hdr, (uint32_t)ci + 1);
-                MOE_TOC(tid == 0, 18, t_w);
-                MOE_TIC(t_c);
-                const uint8_t *sg = ring + (size_t)s0 * p.slot_bytes;
-                const uint8_t *su = ring + (size_t)s1 * p.slot_bytes;
-                float dg0[4] = {0.f, 0.f, 0.f, 0.f}, dg1[4] = {0.f, 0.f, 0.f, 0.f};
-                float du0[4] = {0.f, 0.f, 0.f, 0.f}, du1[4] = {0.f, 0.f, 0.f, 0.f};
-                if (ok0 && ok1) {
-#pragma unroll
-                    for (int m = 0; m < MC_GU; ++m) {
-                        const int c = warp + kConsumerWarps * m;
-                        if (c < nch) {
-                            chunk_mma(sg, sg + gu_pk, H / 2, H / 16, c, g, q, bx[m], dg0, dg1);
-                            chunk_mma(su, su + gu_pk, H / 2, H / 16, c, g, q, bx[m], du0, du1);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&empty[s0]);
-                    mbar_arrive(&empty[s1]);
-                }
-                ci += 2;
-                float dg[4], du[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    dg[i] = dg0[i] + dg1[i];
-                    du[i] = du0[i] + du1[i];
-                }
-                MOE_TOC(tid == 0, 19, t_c);
-                const int rb = claim_red();
-                store_partial(sm.red[rb][warp], dg, g, q, inv0, inv1);
-                store_partial(sm.red[rb][warp] + 128, du, g, q, inv0, inv1);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.red_full[rb]);
-                ++ui;
-            }
-        }
-        MOE_PHASE_MARK(tid == 0, 6);
-        // wait until the epilogue warp has passed the grid barrier (every h written)
-        named_bar(2, kComputeAndEpi);
-        MOE_PHASE_MARK(tid == 0, 7);
-
-        // phase D: down, 32 output rows per unit (two MMA tiles, four chains).
-        // The units of one entry run in an inner loop that only waits,
-        // multiplies and hands the partial sums over; the entry's h
-        // fragments are loaded once before it.
-        {
-            uint32_t bh[MC_D][8][2];
-            float inv0 = 1.f, inv1 = 1.f;
-            int j = d_begin;
-            while (j < d_end) {
-                int entry, K, jend;
-                uint32_t mask;
-                if (j < Sd) {
-                    entry = kSharedEntry;
-                    K = p.Is;
-                    mask = allrows;
-                    jend = min(Sd, d_end);
-                } else {
-                    entry = (j - Sd) / Ho;
-                    K = p.I;
-                    mask = sm.uni.rowmask[entry];
-                    jend = min(Sd + (entry + 1) * Ho, d_end);
-                }
-                const int nch = K / kChunk;
-                const uint32_t rowb = (uint32_t)K / 2, scb = (uint32_t)K / 16;
-                MOE_TIC(t_b);
-                load_b<MC_D>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
-                             (size_t)p.ws.inter_max, mask, nch, warp, kConsumerWarps, lane, bh,
-                             inv0, inv1);
-                MOE_TOC(tid == 0, 21, t_b);
-                for (; j < jend; ++j) {
-                    const int s = rs;
-                    const uint32_t par = rp;
-                    next_slot();
-                    MOE_TIC(t_dw);
-                    const bool ok = ring_wait(&full[s], par, abort, hdr, (uint32_t)ci);
-                    MOE_TOC(tid == 0, 22, t_dw);
-                    MOE_TIC(t_dc);
-                    const uint8_t *st = ring + (size_t)s * p.slot_bytes;
-                    const uint8_t *sc = st + kOutTile * rowb;
-                    float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-                    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (ok) {
-#pragma unroll
-                        for (int m = 0; m < MC_D; ++m) {
-                            const int c = warp + kConsumerWarps * m;
-                            if (c < nch) {
-                                chunk_mma(st, sc, rowb, scb, c, g, q, bh[m], a0, a1);
-                                chunk_mma(st + kTileRows * rowb, sc + kTileRows * scb, rowb, scb, c,
-                                          g, q, bh[m], c0, c1);
-                            }
-                        }
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[s]);
-                    ++ci;
-                    float da[4], dc[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        da[i] = a0[i] + a1[i];
-                        dc[i] = c0[i] + c1[i];
-                    }
-                    MOE_TOC(tid == 0, 23, t_dc);
-                    const int rb = claim_red();
-                    store_partial(sm.red[rb][warp], da, g, q, inv0, inv1);
-                    store_partial(sm.red[rb][warp] + 128, dc, g, q, inv0, inv1);
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&sm.red_full[rb]);
-                    ++ui;
-                }
-            }
-        }
-        MOE_PHASE_MARK(tid == 0, 8);
-        // wait until the epilogue warp has passed the grid barrier (every y written)
-        named_bar(3, kComputeAndEpi);
-        MOE_PHASE_MARK(tid == 0, 12);
-    }
-
-    // ---------------- phase E: blend, spread over the CTAs ----------------
-    // Items (32-row output tile, token row) go to the compute and epilogue
-    // warps of all CTAs, one warp per item, one output per lane.
-    const int items = Ho * p.rows;
-    const int bw = warp == kEpiWarp2 ? kConsumerWarps + 1 : warp;   // blend warp index
-    for (int it = b + G * bw; it < items; it += G * (kConsumerWarps + kEpiWarps)) {
-        const int t = it / p.rows, r = it % p.rows;
-        const int o = t * kOutTile + lane;
-        const float ysv = ld_cg(p.ws.ysbuf + (size_t)r * H + o);
-        float acc = 0.f;
-        // slots in order, eight loads in flight at a time
-        for (int s0 = 0; s0 < k; s0 += 8) {
-            float yv[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                yv[i] = ld_cg(p.ws.ybuf + ((size_t)r * k + min(s0 + i, k - 1)) * H + o);
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (s0 + i < k) acc = fmaf(sm.wts[r * k + s0 + i], yv[i], acc);
-        }
-        if (p.has_shared) acc = fmaf(sm.gate_val[r], ysv, acc);
-        if (!*abort) p.out[(size_t)r * H + o] = f2bf16_rn(acc);
-    }
-    MOE_PHASE_MARK(tid == 0, 9);
-}
-
-// ---------------------------------------------------------------------------
-// Launch
-// ---------------------------------------------------------------------------
-
-template <int A, int B>
-static void *layer_kernel_ptr() {
-    return (void *)moe_layer_kernel<A, B>;
-}
-
-static void *layer_kernel(int mc_gu, int mc_d) {
-    static void *tab[4][4] = {
-        {layer_kernel_ptr<1, 1>(), layer_kernel_ptr<1, 2>(), layer_kernel_ptr<1, 3>(),
-         layer_kernel_ptr<1, 4>()},
-        {layer_kernel_ptr<2, 1>(), layer_kernel_ptr<2, 2>(), layer_kernel_ptr<2, 3>(),
-         layer_kernel_ptr<2, 4>()},
-        {layer_kernel_ptr<3, 1>(), layer_kernel_ptr<3, 2>(), layer_kernel_ptr<3, 3>(),
-         layer_kernel_ptr<3, 4>()},
-        {layer_kernel_ptr<4, 1>(), layer_kernel_ptr<4, 2>(), layer_kernel_ptr<4, 3>(),
-         layer_kernel_ptr<4, 4>()}};
-    if (mc_gu < 1 || mc_gu > 4 || mc_d < 1 || mc_d > 4) return nullptr;
-    return tab[mc_gu - 1][mc_d - 1];
 }
 
 cudaError_t set_layer_smem_limit(int bytes) {
-    for (int a = 1; a <= 4; ++a)
-        for (int b = 1; b <= 4; ++b) {
-            cudaError_t e = cudaFuncSetAttribute(layer_kernel(a, b),
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-            if (e != cudaSuccess) return e;
-        }
+    for (int t = 0; t < 4; ++t)
+        for (int a = 1; a <= 4; ++a)
+            for (int b = 1; b <= 4; ++b) {
+                cudaError_t e = cudaFuncSetAttribute(
+                    layer_kernel(a, b, t), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+                if (e != cudaSuccess) return e;
+            }
     return cudaSuccess;
 }
 
 cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
                          cudaStream_t stream) {
-    void *fn = layer_kernel(mc_gu, mc_d);
+    void *fn = layer_kernel(mc_gu, mc_d, topk_class(p.E));
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kLayerThreads);
+    cfg.blockDim = dim3(kLayerBlockThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];

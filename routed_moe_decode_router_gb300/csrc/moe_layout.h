@@ -18,6 +18,8 @@ constexpr int kOutTile = 32;             // output rows of a down unit / blend t
 constexpr int kChunk = 128;              // inputs per compute-warp chunk
 constexpr int kConsumerWarps = 8;        // compute warps of the layer kernel
 constexpr int kRouteWarps = 8;
+// Layer kernel block: 8 compute warps, 2 epilogue warps, 1 producer warp.
+constexpr int kLayerBlockThreads = (kConsumerWarps + 3) * 32;
 
 // Status word and counters at the start of the workspace (256 bytes).
 struct WsHeader {
