@@ -16,5 +16,11 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def orc():
     from oracle import oracle
+    src = os.environ.get("MOE_ORACLE_MUTANT_SRC")
+    if src:
+        # A mutated copy of the oracle's C source, compiled next to it
+        # (tests/test_oracle_mutants.py runs the pins against such copies).
+        oracle._SRC = src
+        oracle._SO = os.path.join(os.path.dirname(src), "libmoe_oracle.so")
     oracle.build()
     return oracle

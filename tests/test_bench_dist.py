@@ -66,4 +66,4 @@ def test_layer_bytes_decode_matches_closed_form():
     per_expert = 3 * 2048 * 768 * 9 // 16 + 12
     want = 9 * per_expert + 128 * 2048 * 9 // 16 + 4 + 2048 * 2 + 2 * 2048 * 2
     assert bench.layer_bytes(shape, 1, 8) == want
-    assert abs(want / 1e6 - 24.05) < 0.1            # matches the survey's 24.05 MB
+    assert abs(want / 1e6 - 24.05) < 0.1            # 24.05 MB per decode layer-step

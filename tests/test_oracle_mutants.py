@@ -1,0 +1,130 @@
+"""Mutation check of the oracle's pins.
+
+Each mutant is a copy of the oracle's C source with one plausible mistake
+planted by an exact text substitution: a dropped term or factor, a wrong
+sign, exponent bias or index, a transposed operand, a reversed tie-break.
+The copy is compiled on the CPU in a temporary folder and the pin suite
+(tests/test_oracle_pins.py) runs against it in a child process, through the
+``MOE_ORACLE_MUTANT_SRC`` hook of the ``orc`` fixture.  Every mutant must make
+at least one pin fail; an unmutated copy taken through the same route must
+pass them all.  The oracle's own source is only read, never modified.
+"""
+import os
+import re
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ORACLE_SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    # number formats
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e)"),
+    ("e2m1_subnormal_step", "(e == 0) ? 0.5 * m", "(e == 0) ? 1.0 * m"),
+    ("e4m3_exponent_bias", "ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    ("e4m3_subnormal_scale", "ldexp(m / 8.0, -6)", "ldexp(m / 8.0, -7)"),
+    ("e4m3_nan_code_decoded", "if (e == 15 && m == 7)", "if (0)"),
+    ("bf16_round_truncates", "nearbyint(ldexp(a, -qexp))", "floor(ldexp(a, -qexp))"),
+    ("bf16_round_extra_bit", "int qexp = e - 8;", "int qexp = e - 9;"),
+    # NVFP4 matrix layout
+    ("nibble_order_swapped", "(k & 1) ? (byte >> 4) : (byte & 15)",
+     "(k & 1) ? (byte & 15) : (byte >> 4)"),
+    ("scale_block_of_32", "(size_t)(k / 16)]", "(size_t)(k / 32)]"),
+    ("scale2_dropped", "return qs * m->scale2;", "return qs;"),
+    # router
+    ("router_transposed", "w->router_bf16[(size_t)e * H + h]",
+     "w->router_bf16[(size_t)h * E + e]"),
+    ("router_reads_row0", "orc_bf16(x[(size_t)r * H + h])", "orc_bf16(x[h])"),
+    # top-k and routing weights
+    ("topk_ties_to_higher_id", "key[e] > key[best]", "key[e] >= key[best]"),
+    ("softmax_selects_smallest", "key[e] = (double)(float)logit[e];",
+     "key[e] = -(double)(float)logit[e];"),
+    ("softmax_unnormalised", "score[e] = exp(logit[e] - mx) / z;",
+     "score[e] = exp(logit[e] - mx);"),
+    ("sigmoid_sign", "return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
+    ("sigmoid_bias_in_weights", "score[e] = sigmoid64(logit[e]);",
+     "score[e] = sigmoid64(logit[e]) + (double)w->bias[e];"),
+    ("sigmoid_bias_not_in_key",
+     "key[e] = (double)(float)(score[e] + (double)w->bias[e]);",
+     "key[e] = (double)(float)score[e];"),
+    ("norm_over_all_experts", "for (int j = 0; j < k; ++j)\n        sum += score[ids[j]];",
+     "for (int j = 0; j < E; ++j)\n        sum += score[j];"),
+    ("norm_flag_ignored", "if (c->norm_topk_prob)\n            v /= sum;", "v /= sum;"),
+    ("scaling_factor_dropped", "v *= c->routed_scaling_factor;", "v *= 1.0;"),
+    # union
+    ("union_keeps_duplicates", "if (uni[u] == ids[p]) {", "if (0 && uni[u] == ids[p]) {"),
+    ("union_rowmask_slot_bit", "(1u << (p / k))", "(1u << (p % k))"),
+    ("union_slot2u_last_entry", "slot2u[p] = (uint8_t)found;", "slot2u[p] = (uint8_t)(U - 1);"),
+    # expert MLP
+    ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    ("swiglu_operands_swapped", "hbuf[i] = silu64(gs) * us;", "hbuf[i] = gs * silu64(us);"),
+    ("up_reads_gate_matrix", "nvfp4_row(u, H, i, row);", "nvfp4_row(g, H, i, row);"),
+    # whole layer
+    ("expert_ids_transposed", "int e = j->ids[(size_t)r * k + s];",
+     "int e = j->ids[(size_t)s * j->rows + r];"),
+    ("shared_gate_negated", "gate = sigmoid64(dot);", "gate = sigmoid64(-dot);"),
+    ("ungated_shared_halved", "gate = 1.0;", "gate = 0.5;"),
+    ("weighted_sum_unweighted", "acc += wts[(size_t)r * k + j] * y[", "acc += y["),
+    ("weighted_sum_slots_reversed", "y[((size_t)r * per_row + j) * H + o]",
+     "y[((size_t)r * per_row + (k - 1 - j)) * H + o]"),
+    ("shared_term_dropped", "acc += gate * y[", "acc += 0.0 * gate * y["),
+]
+
+
+def _mutate(src: str, old: str, new: str) -> str:
+    assert src.count(old) == 1, "mutation site not unique: %r" % old
+    return src.replace(old, new)
+
+
+def _run_pins(folder: str, text: str):
+    """Compile-check `text` as the oracle source in `folder`, run the pin
+    suite against it; returns (returncode, first failing pin, output tail)."""
+    os.makedirs(folder, exist_ok=True)
+    src = os.path.join(folder, "moe_oracle.c")
+    with open(src, "w") as f:
+        f.write(text)
+    syn = subprocess.run(["gcc", "-fsyntax-only", "-std=c11", "-D_DEFAULT_SOURCE", src],
+                         capture_output=True, text=True)
+    if syn.returncode != 0:
+        return -1, None, syn.stderr[-2000:]
+    # one thread per child: the children run side by side
+    env = dict(os.environ, MOE_ORACLE_MUTANT_SRC=src, OMP_NUM_THREADS="1",
+               OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    p = subprocess.run(
+        [sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+         "-x", "-q", "-p", "no:cacheprovider", "-W", "ignore"],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    out = p.stdout + p.stderr
+    m = re.search(r"FAILED \S+::(\S+)", out)
+    return p.returncode, (m.group(1) if m else None), out[-2000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    base = tmp_path_factory.mktemp("oracle_mutants")
+    with open(ORACLE_SRC) as f:
+        src = f.read()
+    jobs = {"unmutated": src}
+    for name, old, new in MUTANTS:
+        jobs[name] = _mutate(src, old, new)
+    workers = max(1, min(8, os.cpu_count() or 1))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        futs = {name: ex.submit(_run_pins, str(base / name), text)
+                for name, text in jobs.items()}
+        return {name: fut.result() for name, fut in futs.items()}
+
+
+def test_unmutated_copy_passes_the_pins(mutant_results):
+    rc, failed, tail = mutant_results["unmutated"]
+    assert rc == 0, tail
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_pins_reject_mutant(mutant_results, name):
+    rc, failed, tail = mutant_results[name]
+    assert rc != -1, "mutant does not compile:\n" + tail
+    assert rc == 1 and failed is not None, "mutant %s survived the pins:\n%s" % (name, tail)
