@@ -222,6 +222,19 @@ namespace moe {
 // Record a refusal or error for moe_last_error() from another translation
 // unit of the library.
 moe_status set_error(moe_status s, const char *msg) { return fail(s, "%s", msg); }
+
+// Every host check of moe_forward except the workspace's: configuration,
+// rows, weights, x and out.  moe_forward_static runs it before it clears its
+// own workspace, so that a refused call enqueues nothing there either.
+moe_status check_forward_args(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
+                              const uint16_t *out, int rows) {
+    moe_status s;
+    if ((s = check_cfg(cfg)) != MOE_OK || (s = check_rows(cfg, rows)) != MOE_OK ||
+        (s = check_weights(cfg, w, true)) != MOE_OK)
+        return s;
+    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    return check_io(x, out, rows, cfg->hidden);
+}
 }  // namespace moe
 
 extern "C" {
@@ -310,12 +323,9 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
                                size_t ws_bytes, void *stream, void *const *ev) {
     moe_status s;
     WsLayout L;
-    if ((s = check_cfg(cfg)) != MOE_OK || (s = check_rows(cfg, rows)) != MOE_OK ||
-        (s = check_weights(cfg, w, true)) != MOE_OK ||
+    if ((s = moe::check_forward_args(cfg, w, x, out, rows)) != MOE_OK ||
         (s = check_ws(cfg, ws, ws_bytes, &L)) != MOE_OK)
         return s;
-    if (!out) return fail(MOE_ERR_INVALID_ARG, "out is NULL");
-    if ((s = check_io(x, out, rows, cfg->hidden)) != MOE_OK) return s;
     DevInfo *di;
     if ((s = device_info(&di)) != MOE_OK) return s;
 

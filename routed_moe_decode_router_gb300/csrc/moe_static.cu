@@ -10,6 +10,8 @@
 
 namespace moe {
 moe_status set_error(moe_status s, const char *msg);
+moe_status check_forward_args(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
+                              const uint16_t *out, int rows);
 }
 
 namespace {
@@ -49,7 +51,8 @@ moe_status static_ws_address(void **out) {
 extern "C" moe_status moe_forward_static(const moe_config *cfg, const moe_weights *w,
                                          const uint16_t *x, uint16_t *out, int rows,
                                          void *stream) {
-    moe_status s = moe_check_config(cfg);
+    // every argument check first: a refused call enqueues nothing
+    moe_status s = moe::check_forward_args(cfg, w, x, out, rows);
     if (s != MOE_OK) return s;
     const moe::WsLayout L = moe::WsLayout::make(*cfg);
     if (L.total > kStaticWsBytes) {

@@ -129,10 +129,33 @@ def fake_weights():
     return w
 
 
-@pytest.mark.parametrize("case", ["rows0", "rows9", "ids65", "x_null", "overlap",
-                                  "ws_small", "ws_misaligned", "out_null",
-                                  "x_misaligned", "shared_misaligned", "bias_missing"])
+# case -> (expected status, text the error message must contain)
+FORWARD_REFUSALS = {
+    "rows0": (1, "rows=0"),
+    "rows9": (1, "rows=9"),
+    "ids65": (2, "rows*top_k=80 exceeds 64"),
+    "x_null": (1, "x: NULL"),
+    "x_misaligned": (1, "x: NULL or not 16-byte aligned"),
+    "out_null": (1, "out is NULL"),
+    "out_misaligned": (1, "out: not 16-byte aligned"),
+    "overlap": (1, "x and out overlap"),
+    "ws_null": (3, "workspace is NULL"),
+    "ws_small": (3, "needs"),
+    "ws_misaligned": (3, "256-byte aligned"),
+    "router_misaligned": (1, "router_bf16"),
+    "nvfp4_router_null": (1, "router_nvfp4: NULL pointer"),
+    "table_null": (1, "gate expert table: NULL array"),
+    "table_misaligned": (1, "up expert table: misaligned array"),
+    "shared_misaligned": (1, "shared_down_proj: packed/scales must be 16-byte aligned"),
+    "shared_gate_missing": (1, "shared_gate=1 needs"),
+    "bias_missing": (1, "correction_bias"),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FORWARD_REFUSALS))
 def test_forward_refusals_on_host(lib, case):
+    """Each bad argument is refused by its own check, with its own status and
+    message, before anything touches the device (the pointers are fake)."""
     cfg = good_cfg()
     w = fake_weights()
     need = N.moe_workspace_size(cfg)
@@ -146,25 +169,73 @@ def test_forward_refusals_on_host(lib, case):
         rows = 5
     elif case == "x_null":
         x = 0
+    elif case == "x_misaligned":
+        x += 2
+    elif case == "out_null":
+        out = 0
+    elif case == "out_misaligned":
+        out += 8
     elif case == "overlap":
         out = x + 256
+    elif case == "ws_null":
+        ws = 0
     elif case == "ws_small":
         nbytes = need - 1
     elif case == "ws_misaligned":
         ws += 16
-    elif case == "out_null":
-        out = 0
-    elif case == "x_misaligned":
-        x += 2
+    elif case == "router_misaligned":
+        w.router_bf16 = FAKE + 2
+    elif case == "nvfp4_router_null":
+        cfg = good_cfg(router_fmt=1)
+        nbytes = N.moe_workspace_size(cfg)
+        w.router_nvfp4 = N.Nvfp4Desc(0, FAKE, 1.0)
+    elif case == "table_null":
+        w.gate = N.ExpertTable(0, FAKE, FAKE)
+    elif case == "table_misaligned":
+        w.up = N.ExpertTable(FAKE + 4, FAKE, FAKE)
     elif case == "shared_misaligned":
         w.shared_down_proj = N.Nvfp4Desc(FAKE + 8, FAKE, 1.0)
+    elif case == "shared_gate_missing":
+        w.shared_expert_gate = 0
     elif case == "bias_missing":
         cfg = good_cfg(scoring=1, routed_scaling_factor=2.5)
         nbytes = N.moe_workspace_size(cfg)
+    status, text = FORWARD_REFUSALS[case]
     with pytest.raises(N.MoeError) as ei:
         N.moe_forward(cfg, w, x, out, rows, ws, nbytes, 0)
-    assert ei.value.status in (1, 2, 3)
-    assert N.lib().moe_last_error().decode() != ""
+    assert ei.value.status == status, str(ei.value)
+    assert text in N.lib().moe_last_error().decode()
+
+
+@pytest.mark.parametrize("case", ["rows0", "rows9", "x_null", "out_null", "overlap",
+                                  "table_null", "shared_misaligned"])
+def test_static_forward_refuses_before_any_device_call(lib, case):
+    """moe_forward_static checks every argument before it looks up or clears
+    its library-owned workspace, so a bad argument comes back as its own
+    refusal even on a machine without a GPU (a device call there would fail
+    with MOE_ERR_CUDA instead)."""
+    cfg = good_cfg()
+    w = fake_weights()
+    x, out, rows = 0x200000, 0x400000, 2
+    if case == "rows0":
+        rows = 0
+    elif case == "rows9":
+        rows = 9
+    elif case == "x_null":
+        x = 0
+    elif case == "out_null":
+        out = 0
+    elif case == "overlap":
+        out = x + 256
+    elif case == "table_null":
+        w.gate = N.ExpertTable(0, FAKE, FAKE)
+    elif case == "shared_misaligned":
+        w.shared_down_proj = N.Nvfp4Desc(FAKE + 8, FAKE, 1.0)
+    status, text = FORWARD_REFUSALS[case]
+    with pytest.raises(N.MoeError) as ei:
+        N.moe_forward_static(cfg, w, x, out, rows, 0)
+    assert ei.value.status == status, str(ei.value)
+    assert text in N.lib().moe_last_error().decode()
 
 
 def test_route_and_union_refusals_on_host(lib):
