@@ -4,8 +4,9 @@
  * (1..8 token rows).
  *
  * The operation is the routed MoE layer of page "Function forward_moe"
- * (forward_moe(gpu, k, cfg, w, x, out, rows, ws, stream): "Routed MoE over
- * rows rows", with the shared expert run once over all rows) and of page
+ * (forward_moe(gpu, k, cfg, w, x, out, rows, ws, stream), which applies the
+ * routed experts to each of `rows` token rows and runs the shared expert once
+ * for all of them) and of page
  * "metrale_model_layers/layers/moe/forward_token_major.rs"
  * (MoeLayer::forward_token_major_decode: gate projection, batched top-k,
  * gate+up, silu+down, weighted sum + shared-expert blend).  The union of the

@@ -14,9 +14,9 @@
 //   B  every CTA computes the top-k of every row and the union itself, from
 //      the logits in L2 -- the same result in every CTA, so no second
 //      exchange is needed (page "Function forward_moe", RETRACTED and WIDENED
-//      notes: rows * top_k <= 64 ids in one block by pairwise scan, no sort,
-//      nothing sent to the host); the producer then fetches the union
-//      experts' pointer entries.
+//      notes: up to 64 ids, de-duplicated by pairwise comparison in one
+//      block, never sorted or sent to the host); the producer then
+//      fetches the union experts' pointer entries.
 //   C  gate+up sweep: units = 16-row tiles of an entry's gate and up
 //      matrices (shared expert first, then the union experts), CTA b takes
 //      units b, b + G, ...; h = bf16(silu(g) * v) to the workspace

@@ -14,7 +14,7 @@
 // on the logit, sigmoid scoring on sigmoid(logit) + correction bias.
 //
 // Union (page "Function forward_moe", RETRACTED and WIDENED notes): the
-// rows * top_k <= 64 ids resolve in one warp by pairwise scan -- a position
+// (at most 64) ids of all rows are de-duplicated by one warp -- a position
 // starts a union entry when no earlier position holds the same id -- with no
 // sort and no copy to the host.  The same warp writes the device pointer
 // table of the union experts (the forward_moe page's pointer-table upgrade
