@@ -377,6 +377,32 @@ def test_forward_vs_dense_bruteforce(orc, variant):
     assert np.array_equal(res["out_bf16"][exact], want_b[exact])
 
 
+@pytest.mark.parametrize("variant", [
+    dict(num_experts=1, top_k=1),                          # one expert, weight 1
+    dict(num_experts=5, top_k=5),                          # every expert selected
+    dict(num_experts=5, top_k=5, scoring="sigmoid", routed_scaling_factor=2.5,
+         norm_topk_prob=False),
+])
+def test_forward_degenerate_routing_vs_dense_bruteforce(orc, variant):
+    """Routing with no choice left: a single expert, or k = E so that every
+    expert is selected and the weights are the whole (normalised) score
+    vector in descending order."""
+    shape = small_shape(**variant)
+    layer = synth.make_layer(shape, seed=29)
+    x = synth.make_rows(shape, 3, seed=30)
+    res = orc.OracleLayer(layer).forward(x)
+    out, ids, w, _ = brute_forward(layer, ref.to_np(x))
+    assert np.array_equal(res["ids"], ids)
+    for r in range(3):
+        assert sorted(res["ids"][r]) == list(range(shape.num_experts))
+    np.testing.assert_allclose(res["wts"], w, rtol=1e-12)
+    np.testing.assert_allclose(res["out"], out, rtol=1e-10, atol=1e-13)
+    if shape.num_experts == 1:
+        assert np.all(res["wts"] == 1.0)
+    U, uni, _, rowmask = orc.union(res["ids"])
+    assert U == shape.num_experts and np.all(rowmask == 0b111)
+
+
 def test_forward_identical_experts_closed_form(orc):
     """Every routed expert has the same weights: the weighted sum collapses
     to (sum of weights) * y = y (softmax with norm), so
