@@ -31,6 +31,35 @@ def _ptr(t: Optional[torch.Tensor]) -> int:
     return 0 if t is None else t.data_ptr()
 
 
+def _device_of(dl: Optional["DeviceLayer"], ws: "Workspace") -> torch.device:
+    dev = ws.buf.device
+    if dev.type != "cuda":
+        raise ValueError("the workspace is on %s; it must be in CUDA device memory" % dev)
+    if dl is not None and dl.device != dev:
+        raise ValueError("the layer is on %s but the workspace on %s" % (dl.device, dev))
+    return dev
+
+
+def _check_rows(t, name: str, dtype: torch.dtype, cols: int, device: torch.device):
+    """Refuse, before any pointer reaches the library, a [rows, cols] tensor
+    the kernels would misread: wrong dtype or width, not contiguous, or not
+    in memory of the layer's CUDA device (a host pointer handed to a kernel
+    faults the GPU instead of raising).  Reads tensor attributes only, so it
+    is safe inside CUDA graph capture.  The row count itself is checked by
+    the library."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise ValueError("%s has dtype %s, expected %s" % (name, t.dtype, dtype))
+    if t.dim() != 2 or t.shape[1] != cols:
+        raise ValueError("%s has shape %s, expected [rows, %d]" % (name, tuple(t.shape), cols))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if t.device != device:
+        raise ValueError("%s is on %s; the layer and workspace are on %s"
+                         % (name, t.device, device))
+
+
 def _stream(stream: Optional[torch.cuda.Stream]) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -48,6 +77,7 @@ class DeviceLayer:
             layer = layer.to(device)
         self.layer = layer
         self.shape = layer.shape
+        self.device = layer.gate.packed.device
         s = self.shape
         E = s.num_experts
         self._tables = {}
@@ -111,10 +141,14 @@ def forward(dl: DeviceLayer, x: torch.Tensor, ws: Workspace,
             out: Optional[torch.Tensor] = None, per_row_mode: bool = False,
             stream=None) -> torch.Tensor:
     """out[rows, H] (bf16) = routed MoE layer of x[rows, H] (bf16)."""
-    rows, H = x.shape
-    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    dev = _device_of(dl, ws)
+    _check_rows(x, "x", torch.bfloat16, dl.shape.hidden, dev)
+    rows = x.shape[0]
     if out is None:
         out = torch.empty_like(x)
+    _check_rows(out, "out", torch.bfloat16, dl.shape.hidden, dev)
+    if out.shape[0] != rows:
+        raise ValueError("out has %d rows, x has %d" % (out.shape[0], rows))
     N.moe_forward(dl.config(per_row_mode), dl.weights, x.data_ptr(), out.data_ptr(),
                   rows, ws.ptr, ws.nbytes, _stream(stream))
     return out
@@ -123,6 +157,7 @@ def forward(dl: DeviceLayer, x: torch.Tensor, ws: Workspace,
 def route(dl: DeviceLayer, x: torch.Tensor, ws: Workspace, stream=None):
     """Router + top-k: (ids [rows, k] int32, wts [rows, k] fp32,
     logits [rows, E] fp32)."""
+    _check_rows(x, "x", torch.bfloat16, dl.shape.hidden, _device_of(dl, ws))
     rows = x.shape[0]
     k, E = dl.shape.top_k, dl.shape.num_experts
     ids = torch.empty((rows, k), dtype=torch.int32, device=x.device)
@@ -150,6 +185,7 @@ def _union_from_bytes(raw: torch.Tensor) -> dict:
 def union(dl: Optional[DeviceLayer], cfg: N.MoeConfig, ids: torch.Tensor,
           ws: Workspace, stream=None) -> dict:
     """Union of ids [rows, k] (device int32) built on the device."""
+    _check_rows(ids, "ids", torch.int32, cfg.top_k, _device_of(dl, ws))
     rows = ids.shape[0]
     raw = torch.empty(C.sizeof(N.UnionTable), dtype=torch.uint8, device=ids.device)
     N.moe_union(cfg, dl.weights if dl is not None else None, ids.data_ptr(), rows,

@@ -259,3 +259,51 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(N, "library_path", lambda: str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         N.lib()
+
+
+def _cpu_layer_and_workspaces():
+    import types
+    import torch
+    shape = synth.WORKLOADS["tiny_h256_e16"].shape
+    dl = L.DeviceLayer(synth.make_layer(shape, 0), device="cpu")
+    # stand-ins with the attributes the helpers read; nothing reaches a GPU
+    ws_cpu = types.SimpleNamespace(buf=torch.empty(256, dtype=torch.uint8), ptr=0x800000,
+                                   nbytes=1 << 20)
+    ws_cuda = types.SimpleNamespace(buf=types.SimpleNamespace(device=torch.device("cuda:0")),
+                                    ptr=0x800000, nbytes=1 << 20)
+    return shape, dl, ws_cpu, ws_cuda
+
+
+def test_python_helpers_refuse_host_memory_before_calling_the_library(monkeypatch):
+    """layer.forward / route / union refuse tensors that are not in the
+    layer's CUDA memory, of the wrong dtype or width, or not contiguous,
+    before any pointer reaches the library (a host pointer in a kernel
+    would fault the GPU rather than raise)."""
+    import torch
+    shape, dl, ws_cpu, ws_cuda = _cpu_layer_and_workspaces()
+    called = []
+    for name in ("moe_forward", "moe_route", "moe_union"):
+        monkeypatch.setattr(N, name, lambda *a, _n=name: called.append(_n))
+    x = synth.make_rows(shape, 2, seed=1)
+    # a workspace in host memory
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        L.forward(dl, x, ws_cpu)
+    # layer on the host, workspace on a CUDA device
+    with pytest.raises(ValueError, match="the layer is on cpu"):
+        L.forward(dl, x, ws_cuda)
+    dl.device = torch.device("cuda:0")          # as if the layer were resident
+    with pytest.raises(ValueError, match="x is on cpu"):
+        L.forward(dl, x, ws_cuda)
+    with pytest.raises(ValueError, match="dtype"):
+        L.forward(dl, x.float(), ws_cuda)
+    with pytest.raises(ValueError, match="expected \\[rows, 256\\]"):
+        L.forward(dl, x[:, :128], ws_cuda)
+    with pytest.raises(ValueError, match="expected \\[rows, 256\\]"):
+        L.route(dl, x.reshape(-1), ws_cuda)
+    with pytest.raises(ValueError, match="contiguous"):
+        L.forward(dl, torch.empty((256, 2), dtype=torch.bfloat16).t(), ws_cuda)
+    with pytest.raises(ValueError, match="ids has dtype"):
+        L.union(None, dl.cfg, torch.zeros((2, 4), dtype=torch.int64), ws_cuda)
+    with pytest.raises(ValueError, match="ids is on cpu"):
+        L.union(None, dl.cfg, torch.zeros((2, 4), dtype=torch.int32), ws_cuda)
+    assert called == []
