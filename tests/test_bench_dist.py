@@ -113,3 +113,58 @@ def test_layer_bytes_variant_terms():
                                             routed_scaling_factor=2.5), 2, 5) - b0 == E * 4
     assert bench.layer_bytes(base, 2, 6) - b0 == expert
     assert bench.layer_bytes(base, 3, 5) - b0 == 2 * H * 2
+
+
+class _FakeSmi:
+    """Stands in for the nvidia-smi child process of ClockSampler."""
+
+    def __init__(self, out):
+        self.out = out
+
+    def terminate(self):
+        pass
+
+    def kill(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.out, ""
+
+
+def test_clock_sampler_median_max_and_reasons():
+    import bench
+    s = bench.ClockSampler(0)
+    s.proc = _FakeSmi(
+        "0, 2070, 2070, 900.1, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+        "0, 1980, 2070, 1390.2, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+        "0, 2070, 2070, 1000.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active\n"
+        "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+        "a truncated line\n")
+    assert s.stop() == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0,
+                        "reasons": ["sw_power_cap"], "samples": 3}
+    s.proc = _FakeSmi(
+        "0, 1410, 2070, 700.0, 0x0000000000000008, Active, Not Active, Not Active, Not Active\n"
+        "0, 1395, 2070, 690.0, 0x0000000000000048, Active, Active, Not Active, Not Active\n")
+    r = s.stop()
+    assert r["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"] and r["sm_mhz"] == 1402.5
+    s.proc = None
+    assert s.stop()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_committed_traffic_keyed_to_kernel_workload_rows_and_sources(tmp_path, monkeypatch):
+    import bench
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "k.md").write_text(
+        "text\nbench-traffic: kernel=moe_layer_kernel workload=decode_h2048_e128 rows=1 "
+        "bytes_per_launch=24182016 src=abc123\n")
+    (tmp_path / "profiles" / "raw.ncu-rep").write_text(
+        "bench-traffic: kernel=moe_layer_kernel workload=w rows=1 bytes_per_launch=1 src=abc123\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc123")
+    assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1) == 24182016
+    assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 8) is None
+    assert bench.committed_traffic("moe_layer_kernel", "prefill8_h2048_e512", 1) is None
+    assert bench.committed_traffic("moe_route_kernel", "decode_h2048_e128", 1) is None
+    assert bench.committed_traffic("moe_layer_kernel", "w", 1) is None   # only .md / .txt
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "def456")  # sources changed
+    assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1) is None
