@@ -168,3 +168,53 @@ def test_committed_traffic_keyed_to_kernel_workload_rows_and_sources(tmp_path, m
     assert bench.committed_traffic("moe_layer_kernel", "w", 1) is None   # only .md / .txt
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "def456")  # sources changed
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1) is None
+
+
+def test_reference_arm_json_line_on_cpu():
+    """`bench.py --impl reference` times the CPU oracle and prints one JSON
+    line with the contract's keys; it needs no GPU, so it runs here on the
+    small workload."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny_h256_e16", "--steps", "3", "--warmup", "3"],
+                       cwd=root, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 1
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["higher_is_better"] is False
+    assert d["unit"] == "us/layer-step" and d["value"] > 0
+    assert abs(d["ms_per_step"] - d["value"] / 1000.0) < 1e-3
+    assert d["config"]["workload"] == "tiny_h256_e16"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"],
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_under_torchrun_prints_once_from_rank0():
+    """With two ranks, rank 0 alone times the oracle and prints the line
+    (n_gpus = 2); the other rank exits 0 without work."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    p = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+                        "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
+                        "--master-port", str(port), os.path.join(root, "bench.py"),
+                        "--gpus", "2", "--impl", "reference", "--workload", "tiny_h256_e16",
+                        "--steps", "3", "--warmup", "3"],
+                       cwd=root, capture_output=True, text=True, timeout=300)
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [l for l in p.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
