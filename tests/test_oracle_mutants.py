@@ -30,6 +30,11 @@ MUTANTS = [
     ("e4m3_nan_code_decoded", "if (e == 15 && m == 7)", "if (0)"),
     ("bf16_round_truncates", "nearbyint(ldexp(a, -qexp))", "floor(ldexp(a, -qexp))"),
     ("bf16_round_extra_bit", "int qexp = e - 8;", "int qexp = e - 9;"),
+    ("bf16_subnormal_quantum", "if (qexp < -133)              /* quantum of the bfloat16 subnormals */\n        qexp = -133;",
+     "if (qexp < -132)              /* quantum of the bfloat16 subnormals */\n        qexp = -132;"),
+    ("bf16_overflow_threshold", "if (q > 0x1.FEp127)", "if (q > 0x1.FCp127)"),
+    ("bf16_nan_to_infinity", "return 0x7FC0;", "return 0x7F80;"),
+    ("e2m1_sign_dropped", "    return sign ? -mag : mag;\n}\n\n/* FP8", "    return mag;\n}\n\n/* FP8"),
     # NVFP4 matrix layout
     ("nibble_order_swapped", "(k & 1) ? (byte >> 4) : (byte & 15)",
      "(k & 1) ? (byte & 15) : (byte >> 4)"),
@@ -39,8 +44,14 @@ MUTANTS = [
     ("router_transposed", "w->router_bf16[(size_t)e * H + h]",
      "w->router_bf16[(size_t)h * E + e]"),
     ("router_reads_row0", "orc_bf16(x[(size_t)r * H + h])", "orc_bf16(x[h])"),
+    ("nvfp4_router_row0", "nvfp4_row(&w->router_fp4, H, e, wr);",
+     "nvfp4_row(&w->router_fp4, H, 0, wr);"),
     # top-k and routing weights
     ("topk_ties_to_higher_id", "key[e] > key[best]", "key[e] >= key[best]"),
+    ("topk_repeats_an_expert", "            if (taken[e])\n                continue;\n", ""),
+    ("softmax_key_in_fp64", "key[e] = (double)(float)logit[e];", "key[e] = logit[e];"),
+    ("sigmoid_key_in_fp64", "key[e] = (double)(float)(score[e] + (double)w->bias[e]);",
+     "key[e] = score[e] + (double)w->bias[e];"),
     ("softmax_selects_smallest", "key[e] = (double)(float)logit[e];",
      "key[e] = -(double)(float)logit[e];"),
     ("softmax_unnormalised", "score[e] = exp(logit[e] - mx) / z;",
@@ -59,14 +70,18 @@ MUTANTS = [
     ("union_keeps_duplicates", "if (uni[u] == ids[p]) {", "if (0 && uni[u] == ids[p]) {"),
     ("union_rowmask_slot_bit", "(1u << (p / k))", "(1u << (p % k))"),
     ("union_slot2u_last_entry", "slot2u[p] = (uint8_t)found;", "slot2u[p] = (uint8_t)(U - 1);"),
+    ("union_rowmask_not_cleared", "            rowmask[U] = 0;\n", ""),
     # expert MLP
     ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     ("swiglu_operands_swapped", "hbuf[i] = silu64(gs) * us;", "hbuf[i] = gs * silu64(us);"),
     ("up_reads_gate_matrix", "nvfp4_row(u, H, i, row);", "nvfp4_row(g, H, i, row);"),
+    ("down_row_wraps_at_inner_size", "nvfp4_row(d, I, o, row);", "nvfp4_row(d, I, o % I, row);"),
     # whole layer
     ("expert_ids_transposed", "int e = j->ids[(size_t)r * k + s];",
      "int e = j->ids[(size_t)s * j->rows + r];"),
+    ("expert_reads_row0", "const double *xr = j->x + (size_t)r * H;", "const double *xr = j->x;"),
     ("shared_gate_negated", "gate = sigmoid64(dot);", "gate = sigmoid64(-dot);"),
+    ("shared_gate_vector_elem0", "orc_bf16(w->sh_gate_vec[h])", "orc_bf16(w->sh_gate_vec[0])"),
     ("ungated_shared_halved", "gate = 1.0;", "gate = 0.5;"),
     ("weighted_sum_unweighted", "acc += wts[(size_t)r * k + j] * y[", "acc += y["),
     ("weighted_sum_slots_reversed", "y[((size_t)r * per_row + j) * H + o]",

@@ -72,6 +72,27 @@ def test_round_bf16_no_double_rounding(orc):
     assert orc.round_bf16(1e39) == 0x7F80
 
 
+def test_round_bf16_edges_vs_torch(orc):
+    """The ends of the bf16 range against torch's float32 -> bfloat16
+    rounding: the subnormal grid (quantum 2^-133), the largest finite value
+    and the ties above it that overflow to infinity, infinities and NaN."""
+    sub = np.arange(0, 600, dtype=np.float64) * 2.0 ** -135          # 1/4 of the quantum
+    top = np.array([float.fromhex(h) for h in (
+        "0x1.fcp127", "0x1.fdp127", "0x1.fep127", "0x1.fe7ffep127", "0x1.fe8p127",
+        "0x1.ffp127", "0x1.fffffep127")])
+    rng = np.random.default_rng(2)
+    tiny = rng.uniform(0, 2.0 ** -125, 2000)
+    vals = np.concatenate([sub, -sub, top, -top, tiny, [np.inf, -np.inf]])
+    vals = vals.astype(np.float32)
+    want = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([orc.round_bf16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, want)
+    # NaN stays NaN (all exponent bits set, mantissa not zero); its sign and
+    # payload carry no meaning
+    b = orc.round_bf16(float("nan"))
+    assert b & 0x7F80 == 0x7F80 and b & 0x007F != 0
+
+
 def test_nvfp4_elem_vs_library_decode(orc):
     rng = np.random.default_rng(2)
     N, K = 24, 96
@@ -241,6 +262,22 @@ def test_softmax_weights_vs_scipy(orc):
                 assert abs(w.sum() - 1.0) < 1e-13
 
 
+def test_selection_decided_on_fp32_keys(orc):
+    """The top-k decision is taken on keys rounded to fp32, the precision of
+    the kernel's logits: keys that differ only below fp32 resolution tie,
+    and the tie goes to the lower expert id."""
+    shape = small_shape(num_experts=8, top_k=2)
+    ol = orc.OracleLayer(synth.make_layer(shape, seed=31))
+    ids, _ = ol.topk_row(np.array([0.5, 0.5 + 2.0 ** -40, 0.1, 0, 0, 0, 0, 0]))
+    assert list(ids) == [0, 1]
+    # sigmoid(0) = 0.5 and sigmoid(1e-9) = 0.5 + 2.5e-10 round to the same fp32
+    shape = small_shape(num_experts=8, top_k=2, scoring="sigmoid")
+    layer = synth.make_layer(shape, seed=32)
+    layer.bias = torch.zeros(8, dtype=torch.float32)
+    ids, _ = orc.OracleLayer(layer).topk_row(np.array([0.0, 1e-9, -3, -3, -3, -3, -3, -3]))
+    assert list(ids) == [0, 1]
+
+
 def test_softmax_equal_logits_uniform(orc):
     shape = small_shape(num_experts=16, top_k=4)
     ol = orc.OracleLayer(synth.make_layer(shape, seed=11))
@@ -300,6 +337,19 @@ def test_union_vs_python_first_occurrence(orc):
             assert {r for r in range(8) if rowmask[u] >> r & 1} == rows_with
         if rows == 1:
             assert U == k
+
+
+def test_union_ignores_prior_buffer_contents(orc):
+    """The union fills its output arrays whatever they held before."""
+    ids = np.array([[3, 1], [1, 4]], dtype=np.int32)
+    uni = np.full(4, -7, dtype=np.int32)
+    slot2u = np.full((2, 2), 0xEE, dtype=np.uint8)
+    rowmask = np.full(4, 0xFF, dtype=np.uint8)
+    U = orc.lib().orc_union(ids.ctypes.data, 2, 2, uni.ctypes.data, slot2u.ctypes.data,
+                            rowmask.ctypes.data)
+    assert U == 3 and list(uni[:3]) == [3, 1, 4]
+    assert list(rowmask[:3]) == [0b01, 0b11, 0b10]
+    assert slot2u.tolist() == [[0, 1], [1, 2]]
 
 
 def test_union_mean_matches_independent_routing_closed_form(orc):
