@@ -87,6 +87,8 @@ MUTANTS = [
     ("weighted_sum_slots_reversed", "y[((size_t)r * per_row + j) * H + o]",
      "y[((size_t)r * per_row + (k - 1 - j)) * H + o]"),
     ("shared_term_dropped", "acc += gate * y[", "acc += 0.0 * gate * y["),
+    ("output_rounded_through_fp32", "out_bf16[(size_t)r * H + o] = orc_round_bf16(acc);",
+     "out_bf16[(size_t)r * H + o] = orc_round_bf16((double)(float)acc);"),
 ]
 
 

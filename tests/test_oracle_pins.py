@@ -453,6 +453,69 @@ def test_forward_degenerate_routing_vs_dense_bruteforce(orc, variant):
     assert U == shape.num_experts and np.all(rowmask == 0b111)
 
 
+def _bf16_nearest(v: float) -> float:
+    """Nearest bfloat16 to a (normal-range) double, ties to even, by exact
+    rational arithmetic."""
+    from fractions import Fraction
+    if v == 0.0:
+        return 0.0
+    e = math.frexp(abs(v))[1]                 # |v| = f * 2^e, f in [0.5, 1)
+    quantum = Fraction(2) ** (e - 8)          # 8 significant bits
+    return float(round(Fraction(v) / quantum) * quantum)
+
+
+def _bf16_bits(val: float) -> int:
+    return int(np.array([val], dtype=np.float32).view(np.uint32)[0]) >> 16
+
+
+def test_forward_output_rounded_once_to_bf16(orc):
+    """The layer's bf16 output is the nearest bf16 of the fp64 result, not of
+    its fp32 rounding.  One expert, top-1 with norm (weight exactly 1), no
+    shared expert, and a down matrix whose only non-zero weight per row sits
+    at input 0 with value scale2: every output is scale2 * h[0].  scale2 is
+    the fp32 value that puts the product inside the narrow band where fp32
+    rounding lands on a bf16 midpoint, so the two roundings differ."""
+    shape = small_shape(num_experts=1, top_k=1, has_shared=False)
+    layer = synth.make_layer(shape, seed=33)
+    x = synth.make_rows(shape, 1, seed=34)
+    d = dense_mats(layer)
+    xd = torch.as_tensor(ref.bf16_decode(ref.to_np(x))[0], dtype=torch.float64)
+    g = torch.as_tensor(d["gate"][0][0]) @ xd
+    u = torch.as_tensor(d["up"][0][0]) @ xd
+    h0 = float(torch.nn.functional.silu(g) * u)
+    assert abs(h0) > 1e-6
+    found = None
+    for k in range(1, 400):
+        b = _bf16_nearest(abs(h0) * (1 + k / 512))
+        m = b + 2.0 ** (math.frexp(b)[1] - 9)          # midpoint above b
+        c = np.float32(m / abs(h0))
+        for _ in range(4):
+            v = float(c) * h0
+            if (np.float32(v) == np.float32(math.copysign(m, h0)) and abs(v) != m
+                    and abs(abs(v) - m) > 2.0 ** -45 * m
+                    and _bf16_nearest(v) != _bf16_nearest(float(np.float32(v)))):
+                found = (c, v)
+                break
+            c = np.nextafter(c, np.float32(np.inf))
+        if found:
+            break
+    assert found, "no fp32 scale puts the product in the double-rounding band"
+    c, v = found
+    H, I = shape.hidden, shape.moe_inter
+    dn = layer.down
+    dn.packed[0].zero_()
+    dn.scales[0].zero_()
+    dn.packed[0][:, 0] = 2                 # E2M1 code of 1.0 at input 0 (low nibble)
+    dn.scales[0][:, 0] = 0x38              # E4M3 code of 1.0 for inputs 0..15
+    dn.scale2[0] = float(c)
+    res = orc.OracleLayer(layer).forward(x)
+    assert res["wts"][0, 0] == 1.0
+    np.testing.assert_allclose(res["out"][0], v, rtol=1e-13)
+    want = _bf16_bits(_bf16_nearest(v))
+    assert want != _bf16_bits(_bf16_nearest(float(np.float32(v))))
+    assert np.all(res["out_bf16"][0] == want)
+
+
 def test_forward_identical_experts_closed_form(orc):
     """Every routed expert has the same weights: the weighted sum collapses
     to (sum of weights) * y = y (softmax with norm), so
