@@ -80,6 +80,10 @@ MUTANTS = [
     ("expert_ids_transposed", "int e = j->ids[(size_t)r * k + s];",
      "int e = j->ids[(size_t)s * j->rows + r];"),
     ("expert_reads_row0", "const double *xr = j->x + (size_t)r * H;", "const double *xr = j->x;"),
+    ("shared_expert_truncated_to_moe_inter",
+     "orc_expert_mlp(H, c->shared_inter, &j->w->sh_gate",
+     "orc_expert_mlp(H, c->moe_inter < c->shared_inter ? c->moe_inter : c->shared_inter, "
+     "&j->w->sh_gate"),
     ("shared_gate_negated", "gate = sigmoid64(dot);", "gate = sigmoid64(-dot);"),
     ("shared_gate_vector_elem0", "orc_bf16(w->sh_gate_vec[h])", "orc_bf16(w->sh_gate_vec[0])"),
     ("ungated_shared_halved", "gate = 1.0;", "gate = 0.5;"),

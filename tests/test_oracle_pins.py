@@ -409,6 +409,7 @@ def test_forward_reduces_to_swiglu(orc):
     dict(norm_topk_prob=False),
     dict(shared_gated=False),
     dict(has_shared=False),
+    dict(moe_inter=32, shared_inter=96),      # shared expert wider than the routed ones
 ])
 def test_forward_vs_dense_bruteforce(orc, variant):
     shape = small_shape(**variant)
