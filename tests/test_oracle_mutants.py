@@ -40,10 +40,18 @@ MUTANTS = [
      "(k & 1) ? (byte & 15) : (byte >> 4)"),
     ("scale_block_of_32", "(size_t)(k / 16)]", "(size_t)(k / 32)]"),
     ("scale2_dropped", "return qs * m->scale2;", "return qs;"),
+    ("scale_row_stride_halved", "m->scales[(size_t)n * (size_t)(K / 16)",
+     "m->scales[(size_t)n * (size_t)(K / 32)"),
+    ("packed_row_stride_halved", "m->packed[(size_t)n * (size_t)(K / 2)",
+     "m->packed[(size_t)n * (size_t)(K / 4)"),
     # router
     ("router_transposed", "w->router_bf16[(size_t)e * H + h]",
      "w->router_bf16[(size_t)h * E + e]"),
     ("router_reads_row0", "orc_bf16(x[(size_t)r * H + h])", "orc_bf16(x[h])"),
+    ("logits_transposed", "logits[(size_t)r * E + e] = acc;", "logits[(size_t)e * rows + r] = acc;"),
+    ("router_dot_drops_last_input",
+     "            for (int h = 0; h < H; ++h)\n                acc += xr[h] * wr[h];",
+     "            for (int h = 0; h < H - 1; ++h)\n                acc += xr[h] * wr[h];"),
     ("nvfp4_router_row0", "nvfp4_row(&w->router_fp4, H, e, wr);",
      "nvfp4_row(&w->router_fp4, H, 0, wr);"),
     # top-k and routing weights
@@ -56,6 +64,13 @@ MUTANTS = [
      "key[e] = -(double)(float)logit[e];"),
     ("softmax_unnormalised", "score[e] = exp(logit[e] - mx) / z;",
      "score[e] = exp(logit[e] - mx);"),
+    ("softmax_denominator_unshifted", "            z += exp(logit[e] - mx);",
+     "            z += exp(logit[e]);"),
+    ("weight_of_slot_not_expert", "        double v = score[ids[j]];", "        double v = score[j];"),
+    ("norm_sum_drops_last_slot", "    for (int j = 0; j < k; ++j)\n        sum += score[ids[j]];",
+     "    for (int j = 0; j + 1 < k; ++j)\n        sum += score[ids[j]];"),
+    ("bias_of_mirrored_expert", "(double)(float)(score[e] + (double)w->bias[e]);",
+     "(double)(float)(score[e] + (double)w->bias[E - 1 - e]);"),
     ("sigmoid_sign", "return 1.0 / (1.0 + exp(-z));", "return 1.0 / (1.0 + exp(z));"),
     ("sigmoid_bias_in_weights", "score[e] = sigmoid64(logit[e]);",
      "score[e] = sigmoid64(logit[e]) + (double)w->bias[e];"),
@@ -68,6 +83,8 @@ MUTANTS = [
     ("scaling_factor_dropped", "v *= c->routed_scaling_factor;", "v *= 1.0;"),
     # union
     ("union_keeps_duplicates", "if (uni[u] == ids[p]) {", "if (0 && uni[u] == ids[p]) {"),
+    ("union_scan_skips_last_entry", "        for (int u = 0; u < U; ++u)\n            if (uni[u]",
+     "        for (int u = 0; u + 1 < U; ++u)\n            if (uni[u]"),
     ("union_rowmask_slot_bit", "(1u << (p / k))", "(1u << (p % k))"),
     ("union_slot2u_last_entry", "slot2u[p] = (uint8_t)found;", "slot2u[p] = (uint8_t)(U - 1);"),
     ("union_rowmask_not_cleared", "            rowmask[U] = 0;\n", ""),
@@ -75,6 +92,10 @@ MUTANTS = [
     ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     ("swiglu_operands_swapped", "hbuf[i] = silu64(gs) * us;", "hbuf[i] = gs * silu64(us);"),
     ("up_reads_gate_matrix", "nvfp4_row(u, H, i, row);", "nvfp4_row(g, H, i, row);"),
+    ("gate_dot_drops_last_input", "        for (int h = 0; h < H; ++h)\n            gs += row[h] * x[h];",
+     "        for (int h = 0; h < H - 1; ++h)\n            gs += row[h] * x[h];"),
+    ("down_dot_drops_last_input", "        for (int i = 0; i < I; ++i)\n            acc += row[i] * hbuf[i];",
+     "        for (int i = 0; i < I - 1; ++i)\n            acc += row[i] * hbuf[i];"),
     ("down_row_wraps_at_inner_size", "nvfp4_row(d, I, o, row);", "nvfp4_row(d, I, o % I, row);"),
     # whole layer
     ("expert_ids_transposed", "int e = j->ids[(size_t)r * k + s];",
@@ -88,6 +109,8 @@ MUTANTS = [
     ("shared_gate_vector_elem0", "orc_bf16(w->sh_gate_vec[h])", "orc_bf16(w->sh_gate_vec[0])"),
     ("ungated_shared_halved", "gate = 1.0;", "gate = 0.5;"),
     ("weighted_sum_unweighted", "acc += wts[(size_t)r * k + j] * y[", "acc += y["),
+    ("weighted_sum_drops_last_slot", "            for (int j = 0; j < k; ++j)\n                acc += wts",
+     "            for (int j = 0; j + 1 < k; ++j)\n                acc += wts"),
     ("weighted_sum_slots_reversed", "y[((size_t)r * per_row + j) * H + o]",
      "y[((size_t)r * per_row + (k - 1 - j)) * H + o]"),
     ("shared_term_dropped", "acc += gate * y[", "acc += 0.0 * gate * y["),
