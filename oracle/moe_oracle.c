@@ -22,7 +22,7 @@
  *   RETRACTED and WIDENED notes) is reported as a separate result: the union sweep reaches
  *   the per-row result exactly, so the oracle computes per row.
  *
- * Readings of points the pages leave open (all listed in the design notes):
+ * Readings of points the pages leave open:
  *   - NVFP4 matrix [N][K]: packed bytes [N][K/2], low nibble = even input
  *     index; E4M3 (OCP "FN": bias 7, no infinity, S.1111.111 = NaN) scales
  *     [N][K/16], one per 16 contiguous inputs; one fp32 scale2 per matrix.
@@ -392,17 +392,16 @@ static void *orc_worker(void *arg)
  * shared_expert_gate.weight.)
  * The (row, slot) expert evaluations run on `nthreads` POSIX threads; the
  * result does not depend on nthreads. */
-void orc_forward(const orc_cfg *c, const orc_weights *w, const uint16_t *x,
-                 int rows, int nthreads, double *out, uint16_t *out_bf16,
-                 int32_t *ids, double *wts, double *logits)
+static void forward_experts_and_blend(const orc_cfg *c, const orc_weights *w,
+                                      const uint16_t *x, int rows, int nthreads,
+                                      const int32_t *ids, const double *wts,
+                                      double *out, uint16_t *out_bf16)
 {
     const int H = c->hidden, k = c->top_k;
     const int per_row = k + (c->has_shared ? 1 : 0);
     const int ntask = rows * per_row;
     if (nthreads < 1)
         nthreads = 1;
-
-    orc_route(c, w, x, rows, logits, ids, wts);
 
     double *xd = malloc(sizeof(double) * (size_t)rows * H);
     for (size_t i = 0; i < (size_t)rows * H; ++i)
@@ -448,6 +447,76 @@ void orc_forward(const orc_cfg *c, const orc_weights *w, const uint16_t *x,
     free(th);
     free(y);
     free(xd);
+}
+
+void orc_forward(const orc_cfg *c, const orc_weights *w, const uint16_t *x,
+                 int rows, int nthreads, double *out, uint16_t *out_bf16,
+                 int32_t *ids, double *wts, double *logits)
+{
+    orc_route(c, w, x, rows, logits, ids, wts);
+    forward_experts_and_blend(c, w, x, rows, nthreads, ids, wts, out, out_bf16);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The layer at caller-given experts                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Routing weights of caller-given experts sel[0..k-1] of one row (distinct
+ * ids in [0, E)), from the same scores the top-k uses (forward_ep.rs /
+ * forward_token_major.rs: moe_topk_softmax(_batched) with norm_topk_prob,
+ * moe_topk_sigmoid_batched with routed_scaling_factor): softmax over all E
+ * logits, or the unbiased sigmoid; normalised over the k given experts when
+ * norm_topk_prob; times routed_scaling_factor for sigmoid scoring.  With sel
+ * equal to the row's top-k this is exactly the top-k's weights; it exists
+ * to evaluate a row whose selection was decided elsewhere (a near tie that
+ * an fp32 router resolved the other way). */
+void orc_weights_for_ids(const orc_cfg *c, const double *logit,
+                         const int32_t *sel, double *wsel)
+{
+    const int E = c->num_experts, k = c->top_k;
+    double *p = malloc(sizeof(double) * (size_t)E);
+    if (c->scoring == 0) {
+        double top = logit[0];
+        for (int e = 1; e < E; ++e)
+            top = logit[e] > top ? logit[e] : top;
+        double part = 0.0;
+        for (int e = 0; e < E; ++e)
+            part += exp(logit[e] - top);
+        for (int e = 0; e < E; ++e)
+            p[e] = exp(logit[e] - top) / part;
+    } else {
+        for (int e = 0; e < E; ++e)
+            p[e] = 1.0 / (1.0 + exp(-logit[e]));
+    }
+    double tot = 0.0;
+    for (int j = 0; j < k; ++j)
+        tot += p[sel[j]];
+    for (int j = 0; j < k; ++j) {
+        double v = p[sel[j]];
+        v = c->norm_topk_prob ? v / tot : v;
+        wsel[j] = c->scoring == 1 ? v * c->routed_scaling_factor : v;
+    }
+    free(p);
+}
+
+/* The whole layer with the experts of every row given by the caller
+ * (sel[rows][k], in slot order) instead of chosen by the top-k: the router
+ * logits, the weights of orc_weights_for_ids, then the same expert MLPs,
+ * weighted sum and shared-expert blend as orc_forward.  wsel receives the
+ * weights; logits may be NULL. */
+void orc_forward_ids(const orc_cfg *c, const orc_weights *w, const uint16_t *x,
+                     int rows, const int32_t *sel, int nthreads, double *out,
+                     uint16_t *out_bf16, double *wsel, double *logits)
+{
+    const int E = c->num_experts, k = c->top_k;
+    double *lg = logits ? logits : malloc(sizeof(double) * (size_t)rows * E);
+    orc_router_logits(c, w, x, rows, lg);
+    for (int r = 0; r < rows; ++r)
+        orc_weights_for_ids(c, lg + (size_t)r * E, sel + (size_t)r * k,
+                            wsel + (size_t)r * k);
+    forward_experts_and_blend(c, w, x, rows, nthreads, sel, wsel, out, out_bf16);
+    if (!logits)
+        free(lg);
 }
 
 int orc_abi_version(void) { return 1; }

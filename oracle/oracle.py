@@ -94,6 +94,12 @@ def lib():
                                   C.c_void_p, C.c_int, C.c_int, C.c_void_p,
                                   C.c_void_p, C.c_void_p, C.c_void_p,
                                   C.c_void_p]
+        L.orc_weights_for_ids.argtypes = [C.POINTER(Cfg), C.c_void_p,
+                                          C.c_void_p, C.c_void_p]
+        L.orc_forward_ids.argtypes = [C.POINTER(Cfg), C.POINTER(Weights),
+                                      C.c_void_p, C.c_int, C.c_void_p,
+                                      C.c_int, C.c_void_p, C.c_void_p,
+                                      C.c_void_p, C.c_void_p]
         _lib = L
     return _lib
 
@@ -293,4 +299,41 @@ class OracleLayer:
                           int(nthreads), _ptr(out), _ptr(outb), _ptr(ids),
                           _ptr(wts), _ptr(logits))
         return {"out": out, "out_bf16": outb, "ids": ids, "wts": wts,
+                "logits": logits}
+
+    def weights_for_ids(self, logits_row, sel):
+        """Routing weights of the given experts of one row (slot order)."""
+        lr = np.ascontiguousarray(np.asarray(logits_row, dtype=np.float64))
+        sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32))
+        assert sel.shape == (self.shape.top_k,)
+        w = np.zeros(self.shape.top_k, dtype=np.float64)
+        lib().orc_weights_for_ids(C.byref(self.cfg), _ptr(lr), _ptr(sel),
+                                  _ptr(w))
+        return w
+
+    def forward_ids(self, x, sel, nthreads: int = 1) -> dict:
+        """The layer with every row's experts given (sel [rows, k], slot
+        order, distinct ids per row) instead of chosen by the top-k."""
+        x = _np(x).astype(np.uint16, copy=False)
+        rows = x.shape[0]
+        H, E, k = self.shape.hidden, self.shape.num_experts, self.shape.top_k
+        sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32))
+        assert sel.shape == (rows, k)
+        for r in range(rows):
+            if len(set(int(v) for v in sel[r])) != k or sel[r].min() < 0 \
+                    or sel[r].max() >= E:
+                raise ValueError("row %d: ids must be %d distinct experts" % (r, k))
+        if self._subset is not None:
+            missing = set(int(e) for e in sel.ravel()) - self._subset
+            if missing:
+                raise ValueError("experts %s were not copied to the host"
+                                 % sorted(missing))
+        out = np.zeros((rows, H), dtype=np.float64)
+        outb = np.zeros((rows, H), dtype=np.uint16)
+        wts = np.zeros((rows, k), dtype=np.float64)
+        logits = np.zeros((rows, E), dtype=np.float64)
+        lib().orc_forward_ids(C.byref(self.cfg), C.byref(self.w), _ptr(x), rows,
+                              _ptr(sel), int(nthreads), _ptr(out), _ptr(outb),
+                              _ptr(wts), _ptr(logits))
+        return {"out": out, "out_bf16": outb, "ids": sel.copy(), "wts": wts,
                 "logits": logits}

@@ -114,6 +114,18 @@ MUTANTS = [
     ("weighted_sum_slots_reversed", "y[((size_t)r * per_row + j) * H + o]",
      "y[((size_t)r * per_row + (k - 1 - j)) * H + o]"),
     ("shared_term_dropped", "acc += gate * y[", "acc += 0.0 * gate * y["),
+    # the layer at caller-given experts
+    ("given_ids_norm_flag_ignored", "v = c->norm_topk_prob ? v / tot : v;", "v = v / tot;"),
+    ("given_ids_scaling_factor_dropped",
+     "wsel[j] = c->scoring == 1 ? v * c->routed_scaling_factor : v;", "wsel[j] = v;"),
+    ("given_ids_softmax_denominator_unshifted", "part += exp(logit[e] - top);",
+     "part += exp(logit[e]);"),
+    ("given_ids_weight_of_slot_not_expert", "double v = p[sel[j]];", "double v = p[j];"),
+    ("given_ids_norm_sum_of_slots", "tot += p[sel[j]];", "tot += p[j];"),
+    ("given_ids_sigmoid_sign", "p[e] = 1.0 / (1.0 + exp(-logit[e]));",
+     "p[e] = 1.0 / (1.0 + exp(logit[e]));"),
+    ("given_ids_rows_share_row0_weights", "orc_weights_for_ids(c, lg + (size_t)r * E, sel + (size_t)r * k,",
+     "orc_weights_for_ids(c, lg + (size_t)r * E, sel,"),
     ("output_rounded_through_fp32", "out_bf16[(size_t)r * H + o] = orc_round_bf16(acc);",
      "out_bf16[(size_t)r * H + o] = orc_round_bf16((double)(float)acc);"),
 ]

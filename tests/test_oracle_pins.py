@@ -584,3 +584,76 @@ def test_forward_union_sweep_equals_per_row(orc):
                 acc += res["wts"][r, j] * ysw[(int(slot2u[r, j]), r)][o]
             acc += gate * ys[o]
             assert acc == res["out"][r, o]
+
+
+# ---------------------------------------------------------------------------
+# The layer at caller-given experts (used to evaluate a near-tie row at the
+# GPU's selection)
+# ---------------------------------------------------------------------------
+
+def _given_ids(rng, E, k, rows):
+    """Distinct ids per row in a random order, deliberately not the top-k."""
+    return np.stack([rng.permutation(E)[:k] for _ in range(rows)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("variant", [
+    dict(),
+    dict(norm_topk_prob=False),
+    dict(scoring="sigmoid", routed_scaling_factor=2.5),
+    dict(scoring="sigmoid", routed_scaling_factor=1.5, norm_topk_prob=False),
+])
+def test_weights_for_given_ids_vs_scipy(orc, variant):
+    shape = small_shape(num_experts=12, top_k=4, **variant)
+    layer = synth.make_layer(shape, seed=41)
+    ol = orc.OracleLayer(layer, experts=())
+    rng = np.random.default_rng(42)
+    for _ in range(20):
+        lg = rng.normal(0.0, 2.0, shape.num_experts)
+        sel = rng.permutation(shape.num_experts)[:shape.top_k]
+        score = sps.softmax(lg) if shape.scoring == "softmax" else sps.expit(lg)
+        want = score[sel]
+        if shape.norm_topk_prob:
+            want = want / want.sum()
+        if shape.scoring == "sigmoid":
+            want = want * shape.routed_scaling_factor
+        np.testing.assert_allclose(ol.weights_for_ids(lg, sel), want, rtol=1e-13)
+
+
+@pytest.mark.parametrize("variant", [
+    dict(),
+    dict(scoring="sigmoid", routed_scaling_factor=2.5),
+    dict(norm_topk_prob=False, shared_gated=False),
+])
+def test_forward_at_given_ids_vs_dense_bruteforce(orc, variant):
+    """Every row evaluated at experts that are not its top-k, in a random
+    slot order: weights and output against the dense brute force at the
+    same experts."""
+    shape = small_shape(num_experts=9, top_k=3, **variant)
+    layer = synth.make_layer(shape, seed=43)
+    x = synth.make_rows(shape, 4, seed=44)
+    sel = _given_ids(np.random.default_rng(45), shape.num_experts, shape.top_k, 4)
+    res = orc.OracleLayer(layer).forward_ids(x, sel, nthreads=2)
+    d = dense_mats(layer)
+    xd = ref.bf16_decode(ref.to_np(x))
+    logits = xd @ d["router"].T
+    for r in range(4):
+        score = sps.softmax(logits[r]) if shape.scoring == "softmax" else sps.expit(logits[r])
+        w = score[sel[r]]
+        if shape.norm_topk_prob:
+            w = w / w.sum()
+        if shape.scoring == "sigmoid":
+            w = w * shape.routed_scaling_factor
+        np.testing.assert_allclose(res["wts"][r], w, rtol=1e-12)
+        out = sum(w[j] * swiglu64(xd[r], d["gate"][e], d["up"][e], d["down"][e])
+                  for j, e in enumerate(sel[r]))
+        gate = sps.expit(xd[r] @ d["sh_vec"]) if shape.shared_gated else 1.0
+        out = out + gate * swiglu64(xd[r], d["sh_gate"], d["sh_up"], d["sh_down"])
+        np.testing.assert_allclose(res["out"][r], out, rtol=1e-10, atol=1e-13)
+
+
+def test_forward_at_given_ids_refuses_repeated_ids(orc):
+    shape = small_shape(num_experts=9, top_k=3)
+    layer = synth.make_layer(shape, seed=43)
+    x = synth.make_rows(shape, 1, seed=44)
+    with pytest.raises(ValueError):
+        orc.OracleLayer(layer).forward_ids(x, np.array([[1, 1, 2]], dtype=np.int32))
