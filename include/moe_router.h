@@ -77,7 +77,13 @@ typedef enum moe_status {
 #define MOE_DEV_OK 0
 #define MOE_DEV_BAD_EXPERT_ID 1     /* an id outside [0, num_experts) */
 #define MOE_DEV_MISALIGNED_PTR 2    /* an expert matrix not 16-byte aligned */
-#define MOE_DEV_WAIT_TIMEOUT 3      /* an on-chip wait exceeded its bound */
+#define MOE_DEV_WAIT_TIMEOUT 3      /* an on-chip wait exceeded its bound
+                                       (about two seconds); the launch skipped
+                                       the rest of its work.  The workspace
+                                       stays usable as it is: the next launch
+                                       runs its grid barriers on a counter the
+                                       failed launch zeroed, so no
+                                       moe_workspace_init is needed */
 
 enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
 enum { MOE_ROUTER_BF16 = 0, MOE_ROUTER_NVFP4 = 1 };
@@ -167,9 +173,12 @@ MOE_API moe_status moe_check_config(const moe_config *cfg);
  * workspace must be 256-byte aligned. */
 MOE_API size_t moe_workspace_size(const moe_config *cfg);
 
-/* Zero the workspace's counters and status word (async on `stream`).  Call
- * once after allocating a workspace; every later call leaves the counters
- * at zero again. */
+/* Zero the whole workspace, its counters and status word included (async
+ * on `stream`).  Call once after allocating a workspace.  The kernels keep
+ * the counters consistent from then on -- a launch ticket that only grows,
+ * and two grid-barrier counters that alternate between launches, each
+ * zeroed by the launch before the one that uses it -- so no later call,
+ * change of row count or timed-out launch needs a second initialisation. */
 MOE_API moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /* Router + top-k for `rows` rows (forward_token_major.rs: gate projection
@@ -252,8 +261,10 @@ MOE_API moe_status moe_read_routing(const moe_config *cfg, const void *ws,
                             float *wts, moe_union_table *uni, void *stream);
 
 /* Synchronise `stream`, read the workspace's device status word into *code
- * (MOE_DEV_*), and clear it.  Returns MOE_ERR_DEVICE_STATUS when the code is
- * non-zero.  Test and diagnostics use only: it blocks the host. */
+ * (MOE_DEV_*), and clear it (only the status word and its detail: the
+ * counters need no reset, even after MOE_DEV_WAIT_TIMEOUT).  Returns
+ * MOE_ERR_DEVICE_STATUS when the code is non-zero.  Test and diagnostics
+ * use only: it blocks the host. */
 MOE_API moe_status moe_read_device_status(void *ws, size_t ws_bytes, int *code,
                                   void *stream);
 

@@ -97,6 +97,7 @@ struct LayerSmem {
     uint32_t umask[kMaxIds];
     uint64_t red_full[kRed];                    // partials ready (8 compute-warp arrivals)
     uint64_t red_empty[kRed];                   // partials consumed (1 epilogue arrival)
+    unsigned long long *bar;                    // this launch's grid-barrier counter
     int abort;
 };
 
@@ -265,6 +266,13 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     }
     pdl_trigger();
     pdl_wait();
+    // launch ticket (the second epilogue warp is idle in phase A): this
+    // launch's barrier counter, and the next launch's counter zeroed
+    if (warp == kEpiWarp2 && lane == 0) {
+        const unsigned long long n = atomicAdd(&hdr->launch_ticket, 1ULL) / (unsigned)G;
+        sm.bar = &hdr->bar_count[n & 1];
+        if (b == 0) hdr->bar_count[(n + 1) & 1] = 0ULL;
+    }
     MOE_PHASE_MARK(tid == 0, 1);
 
     // ---------------- phase A: router rows ----------------
@@ -343,7 +351,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     }
     __syncthreads();
     MOE_PHASE_MARK(tid == 0, 2);
-    if (tid == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 1u);
+    if (tid == 0) grid_arrive_wait(sm.bar, G, abort, hdr, 1u);
     __syncthreads();
     MOE_PHASE_MARK(tid == 0, 3);
 
@@ -503,7 +511,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         // then release the compute warps
         named_bar(5, kEpiWarps * 32);
         MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 13);
-        if (lane == 0 && epi_idx == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 2u);
+        if (lane == 0 && epi_idx == 0) grid_arrive_wait(sm.bar, G, abort, hdr, 2u);
         named_bar(5, kEpiWarps * 32);
         MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 14);
         asm volatile("bar.arrive 2, %0;" ::"r"(kComputeAndEpi) : "memory");
@@ -569,7 +577,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         }
         named_bar(5, kEpiWarps * 32);
         MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 15);
-        if (lane == 0 && epi_idx == 0) grid_arrive_wait(&hdr->bar_count, G, abort, hdr, 3u);
+        if (lane == 0 && epi_idx == 0) grid_arrive_wait(sm.bar, G, abort, hdr, 3u);
         named_bar(5, kEpiWarps * 32);   // both epilogue warps read y in the blend
         asm volatile("bar.arrive 3, %0;" ::"r"(kComputeAndEpi) : "memory");
     } else {

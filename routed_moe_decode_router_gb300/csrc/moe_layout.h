@@ -22,13 +22,22 @@ constexpr int kRouteWarps = 8;
 constexpr int kLayerBlockThreads = (kConsumerWarps + 3) * 32;
 
 // Status word and counters at the start of the workspace (256 bytes).
+//
+// Every launch of the layer kernel adds exactly one to launch_ticket per CTA,
+// first thing after its dependency wait, so launch n (counted from the last
+// zeroing of the workspace) reads tickets n*G .. n*G + G-1.  Launch n runs
+// its grid barriers on bar_count[n & 1] and zeroes bar_count[(n + 1) & 1]
+// for launch n + 1.  A launch whose barrier wait ran out leaves its own
+// counter misaligned, but the next launch uses the other, freshly zeroed
+// one, so the workspace needs no re-initialisation after a timeout.
 struct WsHeader {
     uint32_t status;        // first MOE_DEV_* fault recorded (0 = none)
     uint32_t status_info;   // detail of that fault (offending id / unit)
     uint32_t route_ticket;  // last-block ticket of the route kernel
     uint32_t pad0;
-    unsigned long long bar_count;  // grid barrier of the layer kernel (monotonic)
-    uint32_t pad[58];
+    unsigned long long launch_ticket;   // CTAs of all layer launches so far
+    unsigned long long bar_count[2];    // grid barriers of even / odd launches
+    uint32_t pad[54];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 

@@ -18,7 +18,8 @@
 // starts a union entry when no earlier position holds the same id -- with no
 // sort and no copy to the host.  The same warp writes the device pointer
 // table of the union experts (the forward_moe page's pointer-table upgrade
-// path), which the expert kernels read.
+// path) into the workspace, for inspection through moe_union; the layer
+// kernel builds its own copy of the table in shared memory.
 #include <cuda_runtime.h>
 
 #include "moe_blocks.cuh"

@@ -82,6 +82,42 @@ def test_top_k_64_single_row():
     G.check_parity(weights, x, res)
 
 
+DEGENERATE_SHAPES = {
+    # every expert selected: the union is all E experts, the weights the
+    # whole normalised score vector in descending order
+    "k_eq_e_softmax": S(hidden=256, num_experts=16, top_k=16, moe_inter=128, shared_inter=128),
+    "k_eq_e_sigmoid_no_norm": S(hidden=256, num_experts=16, top_k=16, moe_inter=128,
+                                shared_inter=256, scoring="sigmoid", routed_scaling_factor=2.5,
+                                norm_topk_prob=False),
+    # a single expert: weight exactly 1 (norm) or its score (no norm)
+    "one_expert": S(hidden=256, num_experts=1, top_k=1, moe_inter=128, shared_inter=128),
+    "one_expert_sigmoid_no_norm": S(hidden=256, num_experts=1, top_k=1, moe_inter=256,
+                                    shared_inter=128, scoring="sigmoid",
+                                    routed_scaling_factor=1.5, norm_topk_prob=False),
+}
+
+
+@pytest.mark.parametrize("name", list(DEGENERATE_SHAPES))
+@pytest.mark.parametrize("rows", [1, 4, 8])
+def test_degenerate_routing_vs_oracle(name, rows):
+    """Routings with no choice left (k = E, or E = 1): oracle parity, every
+    row's union is all E experts, and the union sweep is byte-identical to
+    the per-row mode."""
+    shape = DEGENERATE_SHAPES[name]
+    rows = min(rows, 64 // shape.top_k)
+    weights, x = G.make_case(shape, rows, seed_w=91, seed_x=92)
+    res = G.gpu_run(weights, x)
+    G.check_parity(weights, x, res)
+    assert res["uni"]["U"] == shape.num_experts
+    assert all(m == (1 << rows) - 1 for m in res["uni"]["rowmask"][:shape.num_experts])
+    for r in range(rows):
+        assert sorted(res["ids"][r]) == list(range(shape.num_experts))
+    if shape.num_experts == 1 and shape.norm_topk_prob:
+        assert np.all(res["wts"] == 1.0)
+    pr = G.gpu_run(weights, x, per_row=True)
+    assert torch.equal(res["out"].view(torch.int16), pr["out"].view(torch.int16))
+
+
 @pytest.mark.parametrize("name", ["tiny", "sigmoid_bias", "nvfp4_router", "no_shared",
                                   "i1536_down_w6"])
 @pytest.mark.parametrize("seed", range(6))
@@ -150,23 +186,30 @@ def test_device_status_on_bad_expert_id():
 
 def test_grid_barrier_timeout_sets_status_and_context_survives():
     """A bounded wait that runs out records MOE_DEV_WAIT_TIMEOUT and the
-    context stays usable.  The workspace's grid-barrier counter (header offset
-    16) is skewed to G - 1, so the first CTA at barrier 1 completes it and the
-    other G - 1 wait for arrivals that never come; their waits run out after
-    about two seconds, they skip the rest of the layer, and the launch ends."""
+    context stays usable.  In a fresh workspace the first launch (ticket 0)
+    runs its grid barriers on counter 0 (header offset 24), which is skewed
+    to G - 1: the first CTA at barrier 1 completes it and the other G - 1
+    wait for arrivals that never come; their waits run out after about two
+    seconds, they skip the rest of the layer, and the launch ends.  The same
+    workspace then computes the layer correctly twice more with no
+    re-initialisation: the next launch uses counter 1, which the failed
+    launch zeroed, and the one after it counter 0 again, zeroed by its
+    predecessor."""
     weights, x = G.make_case(TINY, 2, seed_w=31, seed_x=32)
     ws = L.Workspace(TINY)
     grid = torch.cuda.get_device_properties(0).multi_processor_count
-    ws.buf[16:24].view(torch.int64).fill_(grid - 1)
+    torch.cuda.synchronize()
+    assert int(ws.buf[16:24].view(torch.int64).item()) == 0      # launch ticket
+    ws.buf[24:32].view(torch.int64).fill_(grid - 1)
     dl = L.DeviceLayer(weights)
     L.forward(dl, x, ws)
     torch.cuda.synchronize()
     assert ws.status() == 3          # MOE_DEV_WAIT_TIMEOUT
     assert ws.status() == 0          # cleared by the read
-    # a fresh header, and the same workspace computes the layer again
-    N.moe_workspace_init(ws.ptr, ws.nbytes, 0)
-    res = G.gpu_run(weights, x, ws=ws, dl=dl)
-    G.check_parity(weights, x, res)
+    assert int(ws.buf[16:24].view(torch.int64).item()) == grid  # one ticket per CTA
+    for _ in range(2):
+        res = G.gpu_run(weights, x, ws=ws, dl=dl)
+        G.check_parity(weights, x, res)
 
 
 def test_workspace_reuse_across_row_counts():

@@ -5,7 +5,9 @@ These tests give the checker the oracle's own result dressed as a GPU
 result, which it must accept, and then that result with one planted error
 (a wrong expert, a routing weight or an output just past its tolerance, a
 wrong union entry or row mask, a device status), which it must reject.  A
-swap of two experts whose keys tie exactly is accepted as a near tie."""
+swap of two experts whose keys tie exactly is accepted as a near tie only
+where the case allows one, and that row's weights and output are then still
+compared, with the oracle evaluated at the swapped selection."""
 import copy
 
 import numpy as np
@@ -110,16 +112,8 @@ def test_rejects_a_device_status(case):
 def test_near_tie_accepted_only_when_keys_tie():
     """Experts 3 and 9 get identical router rows, so their logits tie
     exactly and the oracle orders them 3 then 9; a GPU result with 9 then 3
-    is a near tie (that row's output is then not compared).  Swapping two
-    experts whose keys differ is an error."""
-    weights = synth.make_layer(SHAPE, seed=43)
-    weights.router_bf16[3] = weights.router_bf16[3] * 4   # make both likely winners
-    weights.router_bf16[9] = weights.router_bf16[3]
-    x = synth.make_rows(SHAPE, 2, seed=44)
-    res, orc = _as_gpu_result(weights, x)
-    rows_with_both = [r for r in range(2) if {3, 9} <= set(int(v) for v in orc["ids"][r])]
-    assert rows_with_both, orc["ids"]
-    r = rows_with_both[0]
+    is a near tie.  Swapping two experts whose keys differ is an error."""
+    weights, x, res, orc, r = _tied_case()
     ids = res["ids"].copy()
     a, b = list(ids[r]).index(3), list(ids[r]).index(9)
     ids[r, a], ids[r, b] = 9, 3
@@ -134,3 +128,53 @@ def test_near_tie_accepted_only_when_keys_tie():
     assert keys[r, ids2[r, j0]] != keys[r, ids2[r, j1]]
     with pytest.raises(AssertionError):
         G.compare_ids(weights, x, ids2, orc["ids"], orc["logits"])
+
+
+def _tied_case():
+    weights = synth.make_layer(SHAPE, seed=43)
+    weights.router_bf16[3] = weights.router_bf16[3] * 4   # make both likely winners
+    weights.router_bf16[9] = weights.router_bf16[3]
+    x = synth.make_rows(SHAPE, 2, seed=44)
+    res, orc = _as_gpu_result(weights, x)
+    rows_with_both = [r for r in range(2) if {3, 9} <= set(int(v) for v in orc["ids"][r])]
+    assert rows_with_both, orc["ids"]
+    return weights, x, res, orc, rows_with_both[0]
+
+
+def _swap_tied(res, r):
+    """The result with experts 3 and 9 (and their weights) swapped in row r,
+    as an fp32 router that resolved the exact tie the other way would give."""
+    bad = copy.deepcopy(res)
+    ids = bad["ids"]
+    a, b = list(ids[r]).index(3), list(ids[r]).index(9)
+    ids[r, a], ids[r, b] = 9, 3
+    bad["wts"][r, a], bad["wts"][r, b] = res["wts"][r, b], res["wts"][r, a]
+    U, uni, slot2u, rowmask = oracle.union(ids)
+    uslot = [[0xFF] * 8 for _ in range(U)]
+    for rr in range(ids.shape[0]):
+        for j in range(ids.shape[1]):
+            uslot[slot2u[rr, j]][rr] = j
+    bad["uni"].update(U=int(U), expert=[int(v) for v in uni], rowmask=[int(v) for v in rowmask],
+                      slot2u=[int(v) for v in slot2u.ravel()], uslot=uslot)
+    return bad
+
+
+def test_near_tie_row_is_still_compared():
+    """The swapped row passes only where the case allows a near tie, and its
+    weights and output are compared with the oracle at the GPU's selection:
+    a wrong output or weight on that row is rejected."""
+    weights, x, res, orc, r = _tied_case()
+    tied = _swap_tied(res, r)
+    st = G.check_parity(weights, x, tied, orc, max_tied=1)
+    assert st["tied_rows"] == [r]
+    with pytest.raises(AssertionError):
+        G.check_parity(weights, x, tied, orc)           # this case allows none
+    bad = copy.deepcopy(tied)
+    bad["out"][r, 7] += 0.05
+    with pytest.raises(AssertionError):
+        G.check_parity(weights, x, bad, orc, max_tied=1)
+    bad = copy.deepcopy(tied)
+    a = list(bad["ids"][r]).index(9)
+    bad["wts"][r, a] = np.float32(bad["wts"][r, a] * (1 + 3e-6))
+    with pytest.raises(AssertionError):
+        G.check_parity(weights, x, bad, orc, max_tied=1)
