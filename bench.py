@@ -16,6 +16,14 @@ runs an independent replica of the workload (the layer has no exchange step
 on one GPU), the timed region is bracketed by barriers and the slowest rank's
 time is reported.  --impl reference times the CPU oracle on the same
 workload (rank 0 only).
+
+The default line is the single-row decode workload (48 layers).  Beside it,
+under "rows_1_to_8", the same measurement (µs per layer-step, mean union,
+roofline fraction of the kernel alone and of the graph step) for the full
+sweep at one and eight rows and for the eight-row prefill sub-chunk with
+independent and with correlated rows.  The CPU-baseline leg times the oracle
+on all host cores and on one, and compares its outputs for the first and
+last timed layers of each workload with the GPU's (the "parity" verdicts).
 """
 from __future__ import annotations
 
@@ -233,47 +241,78 @@ def workload_config(wl, shape, rows, n_layers, extra=None):
     return c
 
 
-def cpu_baseline(layers, xbuf, rows, sample_s, nthreads):
+def oracle_forward(dl, x, nthreads):
+    """The oracle's forward of one layer on host rows x (copies only the
+    experts it selects to the host); returns (result, seconds)."""
+    from oracle import oracle
+    _, ids, _ = oracle.OracleLayer(dl.layer, experts=()).route(x)
+    ol = oracle.OracleLayer(dl.layer, experts=set(int(v) for v in ids.ravel()))
+    t0 = time.perf_counter()
+    res = ol.forward(x, nthreads=nthreads)
+    return res, time.perf_counter() - t0
+
+
+def parity_verdict(pairs):
+    """GPU outputs against the oracle's on the same layers: bf16 out vs fp64
+    out (rel-L2 <= 5e-3, max-abs <= 3e-2, the parity tests' bar) and the
+    selected experts (ids of the workspace's last layer are not kept, so the
+    comparison is on the outputs)."""
+    import numpy as np
+    rel, mab = [], []
+    for got, want in pairs:
+        g = got.float().cpu().numpy().astype(np.float64)
+        rel.append(float(np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30)))
+        mab.append(float(np.abs(g - want).max()))
+    return {"layers_checked": len(pairs), "max_rel_l2": max(rel), "max_abs": max(mab),
+            "ok": bool(max(rel) <= 5e-3 and max(mab) <= 3e-2)}
+
+
+def cpu_baseline(layers, xbuf, outbuf, rows, sample_s, nthreads, sample_1core_s):
     """The oracle as it stands on the host cores: whole layer forwards of
     the same workload, layer after layer, until `sample_s` seconds of oracle
-    time have been spent (setup copies of the selected experts untimed)."""
+    time have been spent (setup copies of the selected experts untimed), then
+    the same on one core for `sample_1core_s`.  The first and last layers'
+    oracle outputs are also compared with the GPU's outputs of the timed
+    region (outbuf), as the parity verdict of the line."""
     from oracle import oracle
     oracle.build()
     spent, n, used = 0.0, 0, 1
+    outs = {}
     for l, dl in enumerate(layers):
         x = xbuf[l].cpu()
-        _, ids, _ = oracle.OracleLayer(dl.layer, experts=()).route(x)
-        ol = oracle.OracleLayer(dl.layer, experts=set(int(v) for v in ids.ravel()))
-        t0 = time.perf_counter()
-        ol.forward(x, nthreads=nthreads)
-        spent += time.perf_counter() - t0
+        res, dt = oracle_forward(dl, x, nthreads)
+        outs[l] = res["out"]
+        spent += dt
         n += 1
         tasks = rows * (dl.shape.top_k + (1 if dl.shape.has_shared else 0))
         used = max(used, min(nthreads, tasks))
         if spent >= sample_s:
             break
+    last = len(layers) - 1
+    if last not in outs:
+        outs[last], _ = oracle_forward(layers[last], xbuf[last].cpu(), nthreads)
+        outs[last] = outs[last]["out"]
+    spent1, n1 = 0.0, 0
+    for l, dl in enumerate(layers):
+        _, dt = oracle_forward(dl, xbuf[l].cpu(), 1)
+        spent1 += dt
+        n1 += 1
+        if spent1 >= sample_1core_s:
+            break
     return {"value": spent / n * 1e6, "unit": UNIT, "cores": used, "kind": "oracle",
             "sample": "%d of the workload's layers, %d row(s) each, whole-layer oracle "
-                      "forwards on %d host threads" % (n, rows, used)}
+                      "forwards on %d host threads" % (n, rows, used),
+            "value_1core": spent1 / n1 * 1e6,
+            "sample_1core": "%d layers on one host thread" % n1,
+            "parity": parity_verdict([(outbuf[0], outs[0]), (outbuf[last], outs[last])])}
 
 
-def run_ours(args, rank, world, local):
+def time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream):
+    """One CUDA graph over every layer of the workload; µs per layer-step of
+    `steps` replays after `warmup` (events on the launching stream).  Returns
+    (graph, elapsed ms, per-layer union sizes)."""
     import torch
     from routed_moe_decode_router_gb300 import layer as L
-    from routed_moe_decode_router_gb300 import native as N
-    import __graft_entry__
-    __graft_entry__.build()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    from routed_moe_decode_router_gb300 import synth
-    wl0 = synth.WORKLOADS[args.workload]
-    rows = args.rows or max(wl0.rows)
-    n_layers = args.layers or wl0.layers
-    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev)
-    ws = L.Workspace(shape, device=dev)
-    stream = torch.cuda.Stream(device=dev)
-
-    # routing of every layer (eager, untimed): union sizes for the byte counts
     U = []
     with torch.cuda.stream(stream):
         for l, dl in enumerate(layers):
@@ -283,18 +322,12 @@ def run_ours(args, rank, world, local):
     stream.synchronize()
     if ws.status() != 0:
         raise RuntimeError("device status set during setup")
-
-    # one CUDA graph over all layers
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for l, dl in enumerate(layers):
             L.forward(dl, xbuf[l], ws, out=outbuf[l])
     torch.cuda.synchronize()
-
-    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
-    sampler.start()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         g.replay()
     torch.cuda.synchronize()
     barrier()
@@ -302,38 +335,123 @@ def run_ours(args, rank, world, local):
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record()
-    for _ in range(args.steps):
+    for _ in range(steps):
         g.replay()
     ev1.record()
     ev1.synchronize()
     torch.cuda.synchronize()
     barrier()
-    clocks = sampler.stop()
-    elapsed = ev0.elapsed_time(ev1)
-    max_elapsed = max_over_ranks(elapsed)
-    value = aggregate_us_per_unit(max_elapsed, args.steps * n_layers, world)
-    ms_per_step = max_elapsed / args.steps
+    return g, ev0.elapsed_time(ev1), U
 
-    # kernel timing pass: the same layers, events around each layer kernel
+
+def time_kernels(layers, xbuf, outbuf, ws, rows, steps, stream):
+    """Mean duration of the layer kernel alone: events recorded around each
+    launch on the launching stream (layers back to back, no overlap)."""
+    import torch
+    from routed_moe_decode_router_gb300 import native as N
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in layers]
     for row in evs:                  # torch creates the CUDA event on first record
         for e in row:
             e.record(stream)
     stream.synchronize()
     kern_ms = 0.0
-    prof_steps = max(1, min(args.steps, 20))
     with torch.cuda.stream(stream):
-        for _ in range(prof_steps):
+        for _ in range(steps):
             for l, dl in enumerate(layers):
                 N.moe_forward_timed(dl.cfg, dl.weights, xbuf[l].data_ptr(),
                                     outbuf[l].data_ptr(), rows, ws.ptr, ws.nbytes,
                                     stream.cuda_stream, [e.cuda_event for e in evs[l]])
             stream.synchronize()
-            for l in range(n_layers):
+            for l in range(len(layers)):
                 kern_ms += evs[l][0].elapsed_time(evs[l][1])
-    launches = prof_steps * n_layers
+    return kern_ms / (steps * len(layers))
+
+
+# Further workloads measured beside the headline line (the metric is quoted
+# for rows = 1..8): the full sweep at one and eight rows, and the eight-row
+# prefill sub-chunk with independent and with correlated rows.  Fewer layers
+# than the full stacks, each still far more distinct weight bytes per step
+# than the 129 MB L2.
+EXTRA_CONFIGS = [
+    ("sweep_h4096_e160", 1, 16, None),
+    ("sweep_h4096_e160", 8, 16, None),
+    ("prefill8_h2048_e512", 8, 16, None),
+    ("prefill8_h2048_e512", 8, 16, "verify_h4096_e256"),
+]
+
+
+def measure_extra(name, rows, n_layers, corr_from, steps, warmup, dev, stream, peak, nthreads,
+                  with_parity):
+    """µs per layer-step, mean union, roofline fractions (kernel alone and
+    graph step) and, on rank 0, the parity verdict of one extra workload."""
+    import torch
+    from routed_moe_decode_router_gb300 import layer as L
+    from routed_moe_decode_router_gb300 import synth
+    wl = synth.WORKLOADS[name]
+    corr = wl.corr if corr_from is None else synth.WORKLOADS[corr_from].corr
+    layers = [L.DeviceLayer(synth.make_layer(wl.shape, wl.seed_base + l, device=dev), device=dev)
+              for l in range(n_layers)]
+    xbuf = torch.empty((n_layers, rows, wl.shape.hidden), dtype=torch.bfloat16, device=dev)
+    for l in range(n_layers):
+        xbuf[l] = synth.make_rows(wl.shape, rows, seed=wl.seed_base + 500 + l, device=dev,
+                                  corr=corr)
+    outbuf = torch.empty_like(xbuf)
+    ws = L.Workspace(wl.shape, device=dev)
+    _, ms, U = time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream)
+    us = ms * 1000.0 / (steps * n_layers)
+    kern_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(steps, 10)), stream)
+    bytes_per_layer = sum(layer_bytes(wl.shape, rows, u) for u in U) / n_layers
+    out = {"workload": name, "rows": rows, "layers": n_layers,
+           "activations": "independent N(0,1)" if corr is None
+           else "correlated rows, a=%.3f" % corr,
+           "us_per_layer_step": round(us, 3), "union_mean": round(sum(U) / len(U), 3),
+           "algorithmic_bytes_per_layer": int(bytes_per_layer),
+           "kernel_us": round(kern_ms * 1000.0, 3),
+           "roofline_frac_kernel": round(bytes_per_layer / (kern_ms * 1e-3) / 1e9 / peak, 4),
+           "roofline_frac_graph": round(bytes_per_layer / (us * 1e-6) / 1e9 / peak, 4),
+           "traffic": committed_traffic("moe_layer_kernel", name, rows)}
+    if with_parity:
+        from oracle import oracle
+        oracle.build()
+        pairs = []
+        for l in (0, n_layers - 1):
+            res, _ = oracle_forward(layers[l], xbuf[l].cpu(), nthreads)
+            pairs.append((outbuf[l], res["out"]))
+        out["parity"] = parity_verdict(pairs)
+    if ws.status() != 0:
+        raise RuntimeError("device status set while timing %s" % name)
+    del layers, xbuf, outbuf, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from routed_moe_decode_router_gb300 import synth
+    wl0 = synth.WORKLOADS[args.workload]
+    rows = args.rows or max(wl0.rows)
+    n_layers = args.layers or wl0.layers
+    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev)
+    from routed_moe_decode_router_gb300 import layer as L
+    ws = L.Workspace(shape, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    g, elapsed, U = time_graph(layers, xbuf, outbuf, ws, rows, args.steps, args.warmup, stream)
+    clocks = sampler.stop()
+    max_elapsed = max_over_ranks(elapsed)
+    value = aggregate_us_per_unit(max_elapsed, args.steps * n_layers, world)
+    ms_per_step = max_elapsed / args.steps
+
+    # kernel timing pass: the same layers, events around each layer kernel
+    kernel_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(args.steps, 20)), stream)
     step_bytes = sum(layer_bytes(shape, rows, u) for u in U)
-    kernel_ms = kern_ms / launches
     peak, peak_kind = hbm_peak()
     achieved = step_bytes / n_layers / (kernel_ms * 1e-3) / 1e9
     traffic = committed_traffic("moe_layer_kernel", args.workload, rows)
@@ -379,16 +497,30 @@ def run_ours(args, rank, world, local):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": peak_kind,
                      "algorithmic_bytes_per_launch": int(step_bytes / n_layers),
-                     "kernel_us": round(kernel_ms * 1000, 3)},
+                     "kernel_us": round(kernel_ms * 1000, 3),
+                     "frac_graph_step": round(layer_gbs / peak, 4),
+                     "note": "frac: the kernel timed alone (events around each launch, no "
+                             "overlap with the previous layer); frac_graph_step: the same "
+                             "bytes over the graph-replayed layer-step, where programmatic "
+                             "dependent launch overlaps consecutive layers"},
         "e2e": {"value": round(e2e_value, 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
                 "d2h_bytes_per_step": int(out_host.numel() * 2)},
         "gpu_launches": n_layers * args.steps,
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(layers, xbuf, rows, args.cpu_sample_s,
-                                            os.cpu_count() or 1)
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if do_cpu:
+        line["cpu_baseline"] = cpu_baseline(layers, xbuf, outbuf, rows, args.cpu_sample_s,
+                                            os.cpu_count() or 1, args.cpu_1core_s)
+    del layers, xbuf, outbuf, ws, g
+    torch.cuda.empty_cache()
+    if not args.no_extra and args.workload == "decode_h2048_e128" and not args.rows \
+            and not args.layers:
+        line["rows_1_to_8"] = [
+            measure_extra(name, r, nl, cf, args.steps, args.warmup, dev, stream, peak,
+                          os.cpu_count() or 1, do_cpu)
+            for name, r, nl, cf in EXTRA_CONFIGS]
     return line
 
 
@@ -460,6 +592,9 @@ def main(argv=None):
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
+    ap.add_argument("--cpu-1core-s", type=float, default=5.0)
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the extra rows=1..8 workloads beside the headline line")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -218,3 +218,19 @@ def test_reference_arm_under_torchrun_prints_once_from_rank0():
     assert len(lines) == 1, p.stdout
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+
+
+def test_parity_verdict_bar():
+    """The bench's parity verdict applies the parity tests' bar: rel-L2 <= 5e-3
+    and max-abs <= 3e-2 of the bf16 output against the fp64 oracle."""
+    import numpy as np
+    import torch
+    import bench
+    want = np.linspace(-1.0, 1.0, 256).reshape(2, 128)
+    ok = bench.parity_verdict([(torch.from_numpy(want).to(torch.bfloat16), want)])
+    assert ok["ok"] and ok["layers_checked"] == 1 and ok["max_rel_l2"] < 5e-3
+    bad = want.copy()
+    bad[1, 7] += 0.05
+    v = bench.parity_verdict([(torch.from_numpy(want).to(torch.bfloat16), want),
+                              (torch.from_numpy(bad).to(torch.bfloat16), want)])
+    assert not v["ok"] and v["max_abs"] > 3e-2
