@@ -307,7 +307,7 @@ def cpu_baseline(layers, xbuf, outbuf, rows, sample_s, nthreads, sample_1core_s)
             "parity": parity_verdict([(outbuf[0], outs[0]), (outbuf[last], outs[last])])}
 
 
-def time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream):
+def time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream, gemv=False):
     """One CUDA graph over every layer of the workload; µs per layer-step of
     `steps` replays after `warmup` (events on the launching stream).  Returns
     (graph, elapsed ms, per-layer union sizes)."""
@@ -316,7 +316,7 @@ def time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream):
     U = []
     with torch.cuda.stream(stream):
         for l, dl in enumerate(layers):
-            L.forward(dl, xbuf[l], ws, out=outbuf[l])
+            L.forward(dl, xbuf[l], ws, out=outbuf[l], gemv=gemv)
             _, _, uni = L.read_routing(dl, ws, rows)
             U.append(uni["U"])
     stream.synchronize()
@@ -325,7 +325,7 @@ def time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for l, dl in enumerate(layers):
-            L.forward(dl, xbuf[l], ws, out=outbuf[l])
+            L.forward(dl, xbuf[l], ws, out=outbuf[l], gemv=gemv)
     torch.cuda.synchronize()
     for _ in range(warmup):
         g.replay()
@@ -344,7 +344,7 @@ def time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream):
     return g, ev0.elapsed_time(ev1), U
 
 
-def time_kernels(layers, xbuf, outbuf, ws, rows, steps, stream):
+def time_kernels(layers, xbuf, outbuf, ws, rows, steps, stream, gemv=False):
     """Mean duration of the layer kernel alone: events recorded around each
     launch on the launching stream (layers back to back, no overlap)."""
     import torch
@@ -358,7 +358,7 @@ def time_kernels(layers, xbuf, outbuf, ws, rows, steps, stream):
     with torch.cuda.stream(stream):
         for _ in range(steps):
             for l, dl in enumerate(layers):
-                N.moe_forward_timed(dl.cfg, dl.weights, xbuf[l].data_ptr(),
+                N.moe_forward_timed(dl.config(gemv=gemv), dl.weights, xbuf[l].data_ptr(),
                                     outbuf[l].data_ptr(), rows, ws.ptr, ws.nbytes,
                                     stream.cuda_stream, [e.cuda_event for e in evs[l]])
             stream.synchronize()
@@ -443,14 +443,16 @@ def run_ours(args, rank, world, local):
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
                            int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
     sampler.start()
-    g, elapsed, U = time_graph(layers, xbuf, outbuf, ws, rows, args.steps, args.warmup, stream)
+    g, elapsed, U = time_graph(layers, xbuf, outbuf, ws, rows, args.steps, args.warmup, stream,
+                               args.gemv)
     clocks = sampler.stop()
     max_elapsed = max_over_ranks(elapsed)
     value = aggregate_us_per_unit(max_elapsed, args.steps * n_layers, world)
     ms_per_step = max_elapsed / args.steps
 
     # kernel timing pass: the same layers, events around each layer kernel
-    kernel_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(args.steps, 20)), stream)
+    kernel_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(args.steps, 20)), stream,
+                             args.gemv)
     step_bytes = sum(layer_bytes(shape, rows, u) for u in U)
     peak, peak_kind = hbm_peak()
     achieved = step_bytes / n_layers / (kernel_ms * 1e-3) / 1e9
@@ -484,6 +486,7 @@ def run_ours(args, rank, world, local):
         "dtype": "f16 mma / f32 accumulate (nvfp4 weights, bf16 activations)",
         "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, bf16 activations)",
         "config": workload_config(wl, shape, rows, n_layers, {
+            "gemv_lever": int(args.gemv and rows == 1),
             "union_mean": round(sum(U) / len(U), 3),
             "l2": "no flush: each step streams %.2f GB of distinct weights (L2 129 MB)"
                   % (step_bytes / 1e9),
@@ -593,6 +596,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-s", type=float, default=10.0)
     ap.add_argument("--cpu-1core-s", type=float, default=5.0)
+    ap.add_argument("--gemv", action="store_true",
+                    help="one-row layers on the CUDA-core GEMV variant (gemv_lever = 1)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the extra rows=1..8 workloads beside the headline line")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)

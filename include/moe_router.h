@@ -58,7 +58,7 @@ extern "C" {
 #define MOE_API
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 #define MOE_MAX_ROWS 8        /* rows per call (forward_moe page, WIDENED note) */
 #define MOE_MAX_IDS 64        /* rows * top_k: one block's pairwise scan */
 #define MOE_MAX_HIDDEN 4096
@@ -118,6 +118,20 @@ typedef struct moe_config {
                                     pair streams its expert separately (the
                                     token-major reference order); the output
                                     is byte-identical to the union mode */
+    int gemv_lever;              /* one-row calls only (rows = 1): 0 = the
+                                    expert projections on the tensor cores
+                                    (NVFP4 unpacked to f16, mma.sync, fp32
+                                    accumulation); 1 = on the CUDA cores as
+                                    a GEMV (f16x2 products and 16-input block
+                                    sums, block scales and the rest of each
+                                    dot product in fp32).  The two give
+                                    results within the parity tolerance of
+                                    each other, not the same bytes; union and
+                                    per-row mode are byte-identical within
+                                    either.  The forward_ep.rs page switches
+                                    its one-row GEMV kernels the same way
+                                    (ctx.levers.gemv_sw).  Rows > 1 ignore
+                                    it. */
 } moe_config;
 
 /* Per-expert NVFP4 matrices: device arrays indexed by expert id

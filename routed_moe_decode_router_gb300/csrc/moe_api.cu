@@ -16,7 +16,7 @@ namespace moe {
 cudaError_t launch_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_union(const UnionParams &p, cudaStream_t stream);
 cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
-                         cudaStream_t stream);
+                         bool gemv, cudaStream_t stream);
 cudaError_t set_layer_smem_limit(int bytes);
 size_t layer_smem_bytes(int stages, uint32_t slot_bytes);
 }  // namespace moe
@@ -111,8 +111,9 @@ moe_status check_cfg(const moe_config *c) {
     if (c->router_fmt != MOE_ROUTER_BF16 && c->router_fmt != MOE_ROUTER_NVFP4)
         return fail(MOE_ERR_INVALID_ARG, "router_fmt=%d: must be bf16 (0) or nvfp4 (1)",
                     c->router_fmt);
-    if ((c->norm_topk_prob | c->shared_gate | c->per_row_mode) & ~1)
-        return fail(MOE_ERR_INVALID_ARG, "norm_topk_prob, shared_gate, per_row_mode are 0/1");
+    if ((c->norm_topk_prob | c->shared_gate | c->per_row_mode | c->gemv_lever) & ~1)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "norm_topk_prob, shared_gate, per_row_mode, gemv_lever are 0/1");
     return MOE_OK;
 }
 
@@ -376,7 +377,8 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     cudaError_t e = cudaSuccess;
     if (ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st);
     if (e == cudaSuccess)
-        e = launch_layer(lp, di->sms, layer_smem_bytes(S, lp.slot_bytes), mc_gu, mc_d, st);
+        e = launch_layer(lp, di->sms, layer_smem_bytes(S, lp.slot_bytes), mc_gu, mc_d,
+                         rows == 1 && cfg->gemv_lever, st);
     if (e == cudaSuccess && ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), st);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "layer launch: %s", cudaGetErrorString(e));
     return ok();

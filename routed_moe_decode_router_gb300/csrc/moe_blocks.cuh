@@ -374,18 +374,74 @@ __device__ __forceinline__ void chunk_mma(const uint8_t *pk, const uint8_t *sc, 
     }
 }
 
+// The one-row CUDA-core variant of chunk_mma (one token row, column 0): the
+// same lane data (rows g and g+8, inputs q*32..+31 of the chunk, their two
+// block scales) and the same B fragments, whose every lane holds token row
+// 0 (load_b with ROW0) scaled so that its largest magnitude lies in
+// [2^8, 2^9).  Each 16-input block's eight f16x2 products are summed in f16
+// (no partial can exceed 8 * 6 * 2^9 < 65504), the block sums are scaled in
+// fp32, and the four lanes of a row are added by shuffles (q order fixed by
+// the butterfly).  ra / rb receive the chunk's dot products of rows g and
+// g+8 with the (scaled) token row.
+__device__ __forceinline__ void chunk_gemv(const uint8_t *pk, const uint8_t *sc, int row_bytes,
+                                           int sc_row_bytes, int c, int g, int q,
+                                           const uint32_t (&b)[8][2], float &ra, float &rb) {
+    const uint4 wa = *reinterpret_cast<const uint4 *>(pk + g * row_bytes + c * 64 + q * 16);
+    const uint4 wb =
+        *reinterpret_cast<const uint4 *>(pk + (g + 8) * row_bytes + c * 64 + q * 16);
+    const uint32_t sa = *reinterpret_cast<const uint16_t *>(sc + g * sc_row_bytes + c * 8 + q * 2);
+    const uint32_t sb =
+        *reinterpret_cast<const uint16_t *>(sc + (g + 8) * sc_row_bytes + c * 8 + q * 2);
+    const uint32_t wA[4] = {wa.x, wa.y, wa.z, wa.w};
+    const uint32_t wB[4] = {wb.x, wb.y, wb.z, wb.w};
+    __half2 acc[2][2];   // [row g / g+8][block 0 / 1]
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) acc[r][k] = __float2half2_rn(0.f);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        uint32_t ha[4], hb[4];
+        e2m1x8_to_f16x2(wA[t], ha);
+        e2m1x8_to_f16x2(wB[t], hb);
+        const uint32_t xv[4] = {b[2 * t][0], b[2 * t][1], b[2 * t + 1][0], b[2 * t + 1][1]};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __half2 x2 = *reinterpret_cast<const __half2 *>(&xv[i]);
+            acc[0][t >> 1] = __hfma2(*reinterpret_cast<const __half2 *>(&ha[i]), x2, acc[0][t >> 1]);
+            acc[1][t >> 1] = __hfma2(*reinterpret_cast<const __half2 *>(&hb[i]), x2, acc[1][t >> 1]);
+        }
+    }
+    const uint32_t fa = e4m3x2_to_f16x2(sa), fb = e4m3x2_to_f16x2(sb);
+    const float2 sca = __half22float2(*reinterpret_cast<const __half2 *>(&fa));
+    const float2 scb = __half22float2(*reinterpret_cast<const __half2 *>(&fb));
+    const float2 a0 = __half22float2(acc[0][0]), a1 = __half22float2(acc[0][1]);
+    const float2 b0 = __half22float2(acc[1][0]), b1 = __half22float2(acc[1][1]);
+    float x = (a0.x + a0.y) * sca.x + (a1.x + a1.y) * sca.y;
+    float y = (b0.x + b0.y) * scb.x + (b1.x + b1.y) * scb.y;
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    ra = x;
+    rb = y;
+}
+
 // B fragments of one token-row matrix (x or h) for this warp's chunks
 // (chunk c = warp + nwarps*m): lane (n = lane/4, q = lane%4) takes row n's 32
 // inputs at c*128 + q*32, in one pass of L2 loads; rows outside `mask` are
 // zero.  The bf16 values are scaled by 2^e (e per row, from the largest
 // magnitude over this warp's chunks) and converted to f16 in place.  inv0 /
 // inv1 receive 2^-e of the D columns 2q and 2q+1.
-template <int MAXC>
+//
+// With ROW0 (the one-row CUDA-core variant) every lane takes token row 0, its
+// largest magnitude goes to [2^8, 2^9) instead, and inv0 = inv1 = 2^-e.
+template <int MAXC, bool ROW0 = false>
 __device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_stride,
                                        uint32_t mask, int nchunk, int warp, int nwarps,
                                        int lane, uint32_t (&b)[MAXC][8][2], float &inv0,
                                        float &inv1) {
-    const int n = lane >> 2, q = lane & 3;
+    const int n = ROW0 ? 0 : lane >> 2, q = lane & 3;
     const bool on = (mask >> n) & 1u;
     // every load first, from a clamped address (row 0 when the row is off,
     // the last chunk when the chunk is past the end), then zero the unused
@@ -422,7 +478,7 @@ __device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_str
                 mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(b[m][s][h])), fabsf(bf16_hi(b[m][s][h]))));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const int e = f16_block_exponent(mx);
+    const int e = ROW0 ? max(f16_block_exponent(mx) - 6, -126) : f16_block_exponent(mx);
     const float up = exp2i(e);
 #pragma unroll
     for (int m = 0; m < MAXC; ++m)
@@ -432,6 +488,10 @@ __device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_str
             for (int h = 0; h < 2; ++h)
                 b[m][s][h] = pack_f16x2(bf16_lo(b[m][s][h]) * up, bf16_hi(b[m][s][h]) * up);
     const float inv = exp2i(-e);
+    if (ROW0) {
+        inv0 = inv1 = inv;
+        return;
+    }
     inv0 = __shfl_sync(0xffffffffu, inv, 8 * q);
     inv1 = __shfl_sync(0xffffffffu, inv, 8 * q + 4);
 }

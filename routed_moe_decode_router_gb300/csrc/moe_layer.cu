@@ -1,7 +1,9 @@
 // moe_layer.cu -- host side of the layer kernel: shared-memory sizing,
-// kernel selection (MC_GU, MC_D, top-k class) and the cooperative, PDL launch.
-// The kernel itself is in moe_layer_kernel.cuh, instantiated in
-// moe_layer_tk0.cu .. moe_layer_tk3.cu.
+// kernel selection (MC_GU, MC_D, top-k class, projection variant) and the
+// cooperative, PDL launch.  The kernel itself is in moe_layer_kernel.cuh,
+// instantiated in moe_layer_tk0.cu .. moe_layer_tk3.cu (tensor-core
+// projections) and moe_layer_tk0_gv.cu .. moe_layer_tk3_gv.cu (the one-row
+// CUDA-core GEMV).
 #include <cuda_runtime.h>
 
 #include "moe_layout.h"
@@ -12,6 +14,10 @@ void *layer_kernel_tk0(int mc_gu, int mc_d);
 void *layer_kernel_tk1(int mc_gu, int mc_d);
 void *layer_kernel_tk2(int mc_gu, int mc_d);
 void *layer_kernel_tk3(int mc_gu, int mc_d);
+void *layer_kernel_tk0_gv(int mc_gu, int mc_d);
+void *layer_kernel_tk1_gv(int mc_gu, int mc_d);
+void *layer_kernel_tk2_gv(int mc_gu, int mc_d);
+void *layer_kernel_tk3_gv(int mc_gu, int mc_d);
 size_t layer_fixed_smem_bytes();
 
 size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
@@ -22,29 +28,31 @@ size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
 // in registers: 4, 8, 16 or two lists of 16).
 static int topk_class(int E) { return E <= 128 ? 0 : (E <= 256 ? 1 : (E <= 512 ? 2 : 3)); }
 
-static void *layer_kernel(int mc_gu, int mc_d, int tk) {
+static void *layer_kernel(int mc_gu, int mc_d, int tk, bool gv) {
     switch (tk) {
-    case 0: return layer_kernel_tk0(mc_gu, mc_d);
-    case 1: return layer_kernel_tk1(mc_gu, mc_d);
-    case 2: return layer_kernel_tk2(mc_gu, mc_d);
-    default: return layer_kernel_tk3(mc_gu, mc_d);
+    case 0: return gv ? layer_kernel_tk0_gv(mc_gu, mc_d) : layer_kernel_tk0(mc_gu, mc_d);
+    case 1: return gv ? layer_kernel_tk1_gv(mc_gu, mc_d) : layer_kernel_tk1(mc_gu, mc_d);
+    case 2: return gv ? layer_kernel_tk2_gv(mc_gu, mc_d) : layer_kernel_tk2(mc_gu, mc_d);
+    default: return gv ? layer_kernel_tk3_gv(mc_gu, mc_d) : layer_kernel_tk3(mc_gu, mc_d);
     }
 }
 
 cudaError_t set_layer_smem_limit(int bytes) {
-    for (int t = 0; t < 4; ++t)
-        for (int a = 1; a <= 4; ++a)
-            for (int b = 1; b <= 4; ++b) {
-                cudaError_t e = cudaFuncSetAttribute(
-                    layer_kernel(a, b, t), cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-                if (e != cudaSuccess) return e;
-            }
+    for (int v = 0; v < 2; ++v)
+        for (int t = 0; t < 4; ++t)
+            for (int a = 1; a <= 4; ++a)
+                for (int b = 1; b <= 4; ++b) {
+                    cudaError_t e = cudaFuncSetAttribute(layer_kernel(a, b, t, v != 0),
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                         bytes);
+                    if (e != cudaSuccess) return e;
+                }
     return cudaSuccess;
 }
 
 cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
-                         cudaStream_t stream) {
-    void *fn = layer_kernel(mc_gu, mc_d, topk_class(p.E));
+                         bool gemv, cudaStream_t stream) {
+    void *fn = layer_kernel(mc_gu, mc_d, topk_class(p.E), gemv);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

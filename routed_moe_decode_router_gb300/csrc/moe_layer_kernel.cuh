@@ -141,8 +141,10 @@ __device__ __forceinline__ void router_decode(const LayerParams &p, int row, uin
 
 // MC_GU / MC_D: B-fragment chunks per compute warp in the gate+up / down
 // phases; TK: the top-k class of the router width (0: E <= 128, 1: <= 256,
-// 2: <= 512, 3: <= 1024), so each instantiation holds one top-k variant.
-template <int MC_GU, int MC_D, int TK>
+// 2: <= 512, 3: <= 1024), so each instantiation holds one top-k variant;
+// GV: the one-row CUDA-core GEMV variant of the expert projections
+// (chunk_gemv) instead of the tensor-core MMA (chunk_mma).
+template <int MC_GU, int MC_D, int TK, bool GV>
 __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const LayerParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     LayerSmem &sm = *reinterpret_cast<LayerSmem *>(smem);
@@ -608,8 +610,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         {
             uint32_t bx[MC_GU][8][2];
             float inv0, inv1;
-            load_b<MC_GU>(p.x, (size_t)H, allrows, H / kChunk, warp, kConsumerWarps, lane, bx,
-                          inv0, inv1);
+            load_b<MC_GU, GV>(p.x, (size_t)H, allrows, H / kChunk, warp, kConsumerWarps, lane,
+                              bx, inv0, inv1);
             MOE_PHASE_MARK(tid == 0, 5);
             named_bar(4, kLayerThreads);
             sweep_layout();
@@ -635,8 +637,18 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     for (int m = 0; m < MC_GU; ++m) {
                         const int c = warp + kConsumerWarps * m;
                         if (c < nch) {
-                            chunk_mma(sg, sg + gu_pk, H / 2, H / 16, c, g, q, bx[m], dg0, dg1);
-                            chunk_mma(su, su + gu_pk, H / 2, H / 16, c, g, q, bx[m], du0, du1);
+                            if constexpr (GV) {
+                                float ga, gb, ua, ub;
+                                chunk_gemv(sg, sg + gu_pk, H / 2, H / 16, c, g, q, bx[m], ga, gb);
+                                chunk_gemv(su, su + gu_pk, H / 2, H / 16, c, g, q, bx[m], ua, ub);
+                                dg0[0] += ga;
+                                dg0[2] += gb;
+                                du0[0] += ua;
+                                du0[2] += ub;
+                            } else {
+                                chunk_mma(sg, sg + gu_pk, H / 2, H / 16, c, g, q, bx[m], dg0, dg1);
+                                chunk_mma(su, su + gu_pk, H / 2, H / 16, c, g, q, bx[m], du0, du1);
+                            }
                         }
                     }
                 }
@@ -691,7 +703,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 const int nch = K / kChunk;
                 const uint32_t rowb = (uint32_t)K / 2, scb = (uint32_t)K / 16;
                 MOE_TIC(t_b);
-                load_b<MC_D>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
+                load_b<MC_D, GV>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
                              (size_t)p.ws.inter_max, mask, nch, warp, kConsumerWarps, lane, bh,
                              inv0, inv1);
                 MOE_TOC(tid == 0, 21, t_b);
@@ -712,9 +724,20 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         for (int m = 0; m < MC_D; ++m) {
                             const int c = warp + kConsumerWarps * m;
                             if (c < nch) {
-                                chunk_mma(st, sc, rowb, scb, c, g, q, bh[m], a0, a1);
-                                chunk_mma(st + kTileRows * rowb, sc + kTileRows * scb, rowb, scb, c,
-                                          g, q, bh[m], c0, c1);
+                                if constexpr (GV) {
+                                    float ya, yb, yc, yd;
+                                    chunk_gemv(st, sc, rowb, scb, c, g, q, bh[m], ya, yb);
+                                    chunk_gemv(st + kTileRows * rowb, sc + kTileRows * scb, rowb,
+                                               scb, c, g, q, bh[m], yc, yd);
+                                    a0[0] += ya;
+                                    a0[2] += yb;
+                                    c0[0] += yc;
+                                    c0[2] += yd;
+                                } else {
+                                    chunk_mma(st, sc, rowb, scb, c, g, q, bh[m], a0, a1);
+                                    chunk_mma(st + kTileRows * rowb, sc + kTileRows * scb, rowb,
+                                              scb, c, g, q, bh[m], c0, c1);
+                                }
                             }
                         }
                     }
@@ -769,18 +792,18 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     MOE_PHASE_MARK(tid == 0, 9);
 }
 
-// The sixteen (MC_GU, MC_D) instantiations of one top-k class.
-template <int TK>
+// The sixteen (MC_GU, MC_D) instantiations of one top-k class and variant.
+template <int TK, bool GV>
 void *layer_kernel_table(int mc_gu, int mc_d) {
     static void *const tab[4][4] = {
-        {(void *)moe_layer_kernel<1, 1, TK>, (void *)moe_layer_kernel<1, 2, TK>,
-         (void *)moe_layer_kernel<1, 3, TK>, (void *)moe_layer_kernel<1, 4, TK>},
-        {(void *)moe_layer_kernel<2, 1, TK>, (void *)moe_layer_kernel<2, 2, TK>,
-         (void *)moe_layer_kernel<2, 3, TK>, (void *)moe_layer_kernel<2, 4, TK>},
-        {(void *)moe_layer_kernel<3, 1, TK>, (void *)moe_layer_kernel<3, 2, TK>,
-         (void *)moe_layer_kernel<3, 3, TK>, (void *)moe_layer_kernel<3, 4, TK>},
-        {(void *)moe_layer_kernel<4, 1, TK>, (void *)moe_layer_kernel<4, 2, TK>,
-         (void *)moe_layer_kernel<4, 3, TK>, (void *)moe_layer_kernel<4, 4, TK>}};
+        {(void *)moe_layer_kernel<1, 1, TK, GV>, (void *)moe_layer_kernel<1, 2, TK, GV>,
+         (void *)moe_layer_kernel<1, 3, TK, GV>, (void *)moe_layer_kernel<1, 4, TK, GV>},
+        {(void *)moe_layer_kernel<2, 1, TK, GV>, (void *)moe_layer_kernel<2, 2, TK, GV>,
+         (void *)moe_layer_kernel<2, 3, TK, GV>, (void *)moe_layer_kernel<2, 4, TK, GV>},
+        {(void *)moe_layer_kernel<3, 1, TK, GV>, (void *)moe_layer_kernel<3, 2, TK, GV>,
+         (void *)moe_layer_kernel<3, 3, TK, GV>, (void *)moe_layer_kernel<3, 4, TK, GV>},
+        {(void *)moe_layer_kernel<4, 1, TK, GV>, (void *)moe_layer_kernel<4, 2, TK, GV>,
+         (void *)moe_layer_kernel<4, 3, TK, GV>, (void *)moe_layer_kernel<4, 4, TK, GV>}};
     if (mc_gu < 1 || mc_gu > 4 || mc_d < 1 || mc_d > 4) return nullptr;
     return tab[mc_gu - 1][mc_d - 1];
 }

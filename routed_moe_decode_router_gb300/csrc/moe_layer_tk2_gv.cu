@@ -1,0 +1,8 @@
+// moe_layer_tk2_gv.cu -- the layer kernel instantiations of top-k class 2
+// with the one-row CUDA-core GEMV expert projections (one translation unit
+// per class and variant, so the eight compile in parallel).
+#include "moe_layer_kernel.cuh"
+
+namespace moe {
+void *layer_kernel_tk2_gv(int mc_gu, int mc_d) { return layer_kernel_table<2, true>(mc_gu, mc_d); }
+}  // namespace moe

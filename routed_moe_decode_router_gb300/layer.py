@@ -14,7 +14,7 @@ from . import native as N
 from .synth import MoeLayerWeights, MoeShape
 
 
-def make_config(shape: MoeShape, per_row_mode: bool = False) -> N.MoeConfig:
+def make_config(shape: MoeShape, per_row_mode: bool = False, gemv: bool = False) -> N.MoeConfig:
     return N.MoeConfig(
         hidden=shape.hidden, num_experts=shape.num_experts,
         router_width=shape.num_experts, top_k=shape.top_k,
@@ -24,7 +24,7 @@ def make_config(shape: MoeShape, per_row_mode: bool = False) -> N.MoeConfig:
         routed_scaling_factor=float(shape.routed_scaling_factor),
         router_fmt=N.MOE_ROUTER_NVFP4 if shape.router_fmt == "nvfp4" else N.MOE_ROUTER_BF16,
         has_shared=int(shape.has_shared), shared_gate=int(shape.shared_gated),
-        per_row_mode=int(per_row_mode))
+        per_row_mode=int(per_row_mode), gemv_lever=int(gemv))
 
 
 def _ptr(t: Optional[torch.Tensor]) -> int:
@@ -112,11 +112,13 @@ class DeviceLayer:
             if s.shared_gated:
                 w.shared_expert_gate = layer.sh_gate_vec.data_ptr()
         self.weights = w
-        self.cfg = make_config(s)
-        self.cfg_per_row = make_config(s, per_row_mode=True)
+        self._cfgs = {(pr, gv): make_config(s, per_row_mode=pr, gemv=gv)
+                      for pr in (False, True) for gv in (False, True)}
+        self.cfg = self._cfgs[(False, False)]
+        self.cfg_per_row = self._cfgs[(True, False)]
 
-    def config(self, per_row_mode: bool = False) -> N.MoeConfig:
-        return self.cfg_per_row if per_row_mode else self.cfg
+    def config(self, per_row_mode: bool = False, gemv: bool = False) -> N.MoeConfig:
+        return self._cfgs[(bool(per_row_mode), bool(gemv))]
 
 
 class Workspace:
@@ -139,7 +141,7 @@ class Workspace:
 
 def forward(dl: DeviceLayer, x: torch.Tensor, ws: Workspace,
             out: Optional[torch.Tensor] = None, per_row_mode: bool = False,
-            stream=None) -> torch.Tensor:
+            stream=None, gemv: bool = False) -> torch.Tensor:
     """out[rows, H] (bf16) = routed MoE layer of x[rows, H] (bf16)."""
     dev = _device_of(dl, ws)
     _check_rows(x, "x", torch.bfloat16, dl.shape.hidden, dev)
@@ -149,7 +151,7 @@ def forward(dl: DeviceLayer, x: torch.Tensor, ws: Workspace,
     _check_rows(out, "out", torch.bfloat16, dl.shape.hidden, dev)
     if out.shape[0] != rows:
         raise ValueError("out has %d rows, x has %d" % (out.shape[0], rows))
-    N.moe_forward(dl.config(per_row_mode), dl.weights, x.data_ptr(), out.data_ptr(),
+    N.moe_forward(dl.config(per_row_mode, gemv), dl.weights, x.data_ptr(), out.data_ptr(),
                   rows, ws.ptr, ws.nbytes, _stream(stream))
     return out
 

@@ -42,7 +42,7 @@ class MoeConfig(C.Structure):
                 ("scoring", C.c_int), ("norm_topk_prob", C.c_int),
                 ("routed_scaling_factor", C.c_float), ("router_fmt", C.c_int),
                 ("has_shared", C.c_int), ("shared_gate", C.c_int),
-                ("per_row_mode", C.c_int)]
+                ("per_row_mode", C.c_int), ("gemv_lever", C.c_int)]
 
 
 class ExpertTable(C.Structure):

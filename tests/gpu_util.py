@@ -32,11 +32,11 @@ OUT_MAX_ABS = 3e-2
 NTHREADS = max(1, min(16, os.cpu_count() or 1))
 
 
-def gpu_run(weights, x, per_row=False, ws=None, dl=None):
+def gpu_run(weights, x, per_row=False, ws=None, dl=None, gemv=False):
     dl = dl or L.DeviceLayer(weights)
     ws = ws or L.Workspace(weights.shape)
     rows = x.shape[0]
-    out = L.forward(dl, x, ws, per_row_mode=per_row)
+    out = L.forward(dl, x, ws, per_row_mode=per_row, gemv=gemv)
     ids, wts, uni = L.read_routing(dl, ws, rows, per_row_mode=per_row)
     torch.cuda.synchronize()
     status = ws.status()

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_abi_version(lib):
-    assert N.moe_abi_version() == 1
+    assert N.moe_abi_version() == 2
 
 
 def test_ctypes_layout_matches_c_header(tmp_path):
@@ -89,6 +89,7 @@ def good_cfg(**kw):
     ("scoring", 7, N.MoeError),
     ("router_fmt", 3, N.MoeError),
     ("per_row_mode", 2, N.MoeError),
+    ("gemv_lever", 2, N.MoeError),
 ])
 def test_config_refusals(lib, field, value, status):
     cfg = good_cfg(**{field: value})

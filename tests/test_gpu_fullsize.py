@@ -54,6 +54,20 @@ def test_full_size_layer_vs_oracle(name, layer, rows, acts):
     assert torch.equal(res["out"].view(torch.int16), pr["out"].view(torch.int16))
 
 
+@pytest.mark.parametrize("name,layer", [("decode_h2048_e128", 3), ("sweep_h4096_e160", 2),
+                                        ("verify_h4096_e256", 4)])
+def test_full_size_gemv_lever_one_row(name, layer):
+    """The one-row CUDA-core GEMV variant at the workloads' full sizes."""
+    wl = synth.WORKLOADS[name]
+    weights = synth.make_layer(wl.shape, wl.seed_base + layer, device="cuda")
+    x = synth.make_rows(wl.shape, 1, seed=wl.seed_base + 500 + layer, device="cuda", corr=wl.corr)
+    res = G.gpu_run(weights, x, gemv=True)
+    st = G.check_parity(weights, x, res)
+    print(name, layer, "gemv", st)
+    pr = G.gpu_run(weights, x, per_row=True, gemv=True)
+    assert torch.equal(res["out"].view(torch.int16), pr["out"].view(torch.int16))
+
+
 def test_full_size_graph_replay_matches_eager():
     wl = synth.WORKLOADS["prefill8_h2048_e512"]
     layers = [L.DeviceLayer(synth.make_layer(wl.shape, wl.seed_base + i, device="cuda"))

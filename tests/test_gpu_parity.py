@@ -280,3 +280,26 @@ def test_layer_chain_on_one_stream_matches_single_calls():
         h = L.forward(dl, h * 8, L.Workspace(shape))
         torch.cuda.synchronize()
         assert torch.equal(h.view(torch.int16), c.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", list(SMALL_SHAPES))
+def test_gemv_lever_one_row_vs_oracle(name):
+    """The one-row CUDA-core GEMV variant (gemv_lever = 1, the forward_ep.rs
+    page's runtime choice between its one-row GEMV kernels): oracle parity,
+    and union mode byte-identical to per-row mode within the variant."""
+    shape = SMALL_SHAPES[name]
+    corr = 0.7 if shape.scoring == "sigmoid" else None
+    for seed in range(2):
+        weights, x = G.make_case(shape, 1, seed_w=61 + seed, seed_x=62 + seed, corr=corr)
+        res = G.gpu_run(weights, x, gemv=True)
+        G.check_parity(weights, x, res)
+        pr = G.gpu_run(weights, x, per_row=True, gemv=True)
+        assert torch.equal(res["out"].view(torch.int16), pr["out"].view(torch.int16))
+
+
+def test_gemv_lever_ignored_above_one_row():
+    shape = SMALL_SHAPES["softmax_is_ne_i"]
+    weights, x = G.make_case(shape, 4, seed_w=63, seed_x=64)
+    a = G.gpu_run(weights, x)
+    b = G.gpu_run(weights, x, gemv=True)
+    assert torch.equal(a["out"].view(torch.int16), b["out"].view(torch.int16))
