@@ -359,11 +359,18 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     lp.sh_down = w->shared_down_proj;
     lp.ws = ws_ptrs(ws, L);
 
+    // Down units of 64 output rows ("wide") when every entry's intermediate
+    // is 2 or 4 chunks of 128: the eight compute warps then split a unit's
+    // chunks and 16-row tiles between them, instead of leaving half of them
+    // without a chunk, and the unit's tile is one copy of twice the size.
+    auto narrow = [](int inter) { return inter == 2 * kChunk || inter == 4 * kChunk; };
+    const bool wide = narrow(cfg->moe_inter) && (!cfg->has_shared || narrow(cfg->shared_inter));
+    lp.down_rows = wide ? 2 * kOutTile : kOutTile;
     // Ring slot = one 16-row gate or up tile (16 x H/2 packed + 16 x H/16
-    // scale bytes) or one 32-row down tile (32 x I/2 + 32 x I/16); a gate+up
-    // unit takes two slots, a down unit one.
+    // scale bytes) or one down tile (down_rows x I/2 + down_rows x I/16); a
+    // gate+up unit takes two slots, a down unit one.
     const size_t gu_slot = (size_t)kTileRows * (cfg->hidden / 2 + cfg->hidden / 16);
-    const size_t d_slot = (size_t)kOutTile * (L.inter_max / 2 + L.inter_max / 16);
+    const size_t d_slot = (size_t)lp.down_rows * (L.inter_max / 2 + L.inter_max / 16);
     lp.slot_bytes = (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot);
     const int budget = di->smem_optin - 1024;
     int S = 16;

@@ -158,8 +158,13 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     const int H = p.H, E = p.E, k = p.k;
     const int It = p.I / kTileRows;
     const int St = p.has_shared ? p.Is / kTileRows : 0;
-    const int Ho = H / kOutTile;                 // down units (32 rows) per entry
-    const int Sd = p.has_shared ? Ho : 0;
+    const int Ho = H / kOutTile;                 // 32-row output tiles (blend)
+    // down units: DR output rows each (32, or 64 when every entry's
+    // intermediate is 2 or 4 chunks wide: "wide" units, whose chunks and
+    // 16-row tiles are spread over all eight compute warps)
+    const int DR = p.down_rows, Hd = H / DR;
+    const bool wide = DR == 2 * kOutTile;
+    const int Sd = p.has_shared ? Hd : 0;
     const bool is_comp = warp < kConsumerWarps;
     const bool is_epi = warp == kEpiWarp || warp == kEpiWarp2;
     const int epi_idx = warp == kEpiWarp2 ? 1 : 0;
@@ -399,7 +404,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     auto sweep_layout = [&]() {
         U = sm.uni.num_union;
         Tgu = St + U * It;
-        Td = Sd + U * Ho;
+        Td = Sd + U * Hd;
         d_begin = (int)((long long)b * Td / G);
         d_end = (int)((long long)(b + 1) * Td / G);
     };
@@ -415,21 +420,21 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 int K;
                 if (j < Sd) {
                     K = p.Is;
-                    dp = p.sh_down.packed + (size_t)j * kOutTile * (K / 2);
-                    ds = p.sh_down.scales + (size_t)j * kOutTile * (K / 16);
+                    dp = p.sh_down.packed + (size_t)j * DR * (K / 2);
+                    ds = p.sh_down.scales + (size_t)j * DR * (K / 16);
                 } else {
-                    const PtrEntry &e = sm.ptrs[(j - Sd) / Ho];
-                    const int tile = (j - Sd) % Ho;
+                    const PtrEntry &e = sm.ptrs[(j - Sd) / Hd];
+                    const int tile = (j - Sd) % Hd;
                     if (e.expert < 0) {
                         ok = issue_empty();
                         continue;
                     }
                     K = p.I;
-                    dp = e.packed[2] + (size_t)tile * kOutTile * (K / 2);
-                    ds = e.scales[2] + (size_t)tile * kOutTile * (K / 16);
+                    dp = e.packed[2] + (size_t)tile * DR * (K / 2);
+                    ds = e.scales[2] + (size_t)tile * DR * (K / 16);
                 }
                 if (!(ok = acquire(pi))) break;
-                issue_pair(dp, ds, kOutTile * K / 2, kOutTile * K / 16);
+                issue_pair(dp, ds, DR * K / 2, DR * K / 16);
             }
             MOE_PHASE_MARK(true, 10);
         }
@@ -517,7 +522,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         named_bar(5, kEpiWarps * 32);
         MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 14);
         asm volatile("bar.arrive 2, %0;" ::"r"(kComputeAndEpi) : "memory");
-        // lane: column col, rows 8 * (rq & 1) .. + 7 of MMA tile rq >> 1
+        // lane: column col, rows 8 * (rq & 1) .. + 7 of MMA tile rq >> 1 (a
+        // 32-row unit), or rows 4 * rq .. + 3 of each of the four MMA tiles
+        // (a wide unit)
         const int half = rq >> 1, r0 = (rq & 1) * 8;
         for (int j = d_begin; j < d_end; ++j, ++ui) {
             if ((ui & 1) != epi_idx) continue;
@@ -533,14 +540,51 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 mask = allrows;
                 s2 = p.sh_down.scale2;
             } else {
-                entry = (j - Sd) / Ho;
-                tile = (j - Sd) % Ho;
+                entry = (j - Sd) / Hd;
+                tile = (j - Sd) % Hd;
                 K = p.I;
                 mask = sm.uni.rowmask[entry];
                 live = sm.ptrs[entry].expert >= 0;
                 s2 = sm.ptrs[entry].scale2[2];
             }
             live = live && ((mask >> col) & 1u);
+            if (wide) {
+                // tile t of the unit comes from the nch warps of tile group
+                // t / tpg (chunks 0..nch-1, in that order), slot t % tpg
+                const int nch = K / kChunk, tpg = nch / 2;
+                const int o = tile * DR + 4 * rq;
+                float *dst = (entry == kSharedEntry)
+                                 ? p.ws.ysbuf + (size_t)col * H + o
+                                 : p.ws.ybuf + ((size_t)col * k + (live ? sm.uni.uslot[entry][col] : 0)) * H + o;
+                const int off = partial_index(col, 4 * rq);
+                ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
+                float4 a[4][4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int w = min((t / tpg) * nch + min(c, nch - 1), kConsumerWarps - 1);
+                        a[t][c] = *reinterpret_cast<const float4 *>(&sm.red[rb][w][(t % tpg) * 128 + off]);
+                    }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.red_empty[rb]);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    float4 v = a[t][0];
+#pragma unroll
+                    for (int c = 1; c < 4; ++c) {
+                        const bool on = c < nch;
+                        v.x += on ? a[t][c].x : 0.f;
+                        v.y += on ? a[t][c].y : 0.f;
+                        v.z += on ? a[t][c].z : 0.f;
+                        v.w += on ? a[t][c].w : 0.f;
+                    }
+                    if (live && !*abort)
+                        *reinterpret_cast<float4 *>(dst + t * kTileRows) =
+                            make_float4(v.x * s2, v.y * s2, v.z * s2, v.w * s2);
+                }
+                continue;
+            }
             const int nwd = min(kConsumerWarps, K / kChunk);   // warps holding down partials
             const int o = tile * kOutTile + half * kTileRows + r0;
             float *dst = (entry == kSharedEntry)
@@ -695,17 +739,20 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     mask = allrows;
                     jend = min(Sd, d_end);
                 } else {
-                    entry = (j - Sd) / Ho;
+                    entry = (j - Sd) / Hd;
                     K = p.I;
                     mask = sm.uni.rowmask[entry];
-                    jend = min(Sd + (entry + 1) * Ho, d_end);
+                    jend = min(Sd + (entry + 1) * Hd, d_end);
                 }
                 const int nch = K / kChunk;
                 const uint32_t rowb = (uint32_t)K / 2, scb = (uint32_t)K / 16;
+                // wide units: this warp's chunk and tile group
+                const int cw = wide ? warp % nch : warp, gw = wide ? warp / nch : 0;
+                const int tpg = nch / 2;
                 MOE_TIC(t_b);
                 load_b<MC_D, GV>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
-                             (size_t)p.ws.inter_max, mask, nch, warp, kConsumerWarps, lane, bh,
-                             inv0, inv1);
+                             (size_t)p.ws.inter_max, mask, nch, cw, wide ? nch : kConsumerWarps,
+                             lane, bh, inv0, inv1);
                 MOE_TOC(tid == 0, 21, t_b);
                 for (; j < jend; ++j) {
                     const int s = rs;
@@ -716,10 +763,31 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     MOE_TOC(tid == 0, 22, t_dw);
                     MOE_TIC(t_dc);
                     const uint8_t *st = ring + (size_t)s * p.slot_bytes;
-                    const uint8_t *sc = st + kOutTile * rowb;
+                    const uint8_t *sc = st + DR * rowb;
                     float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
                     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-                    if (ok) {
+                    if (wide) {
+                        // tiles gw * tpg .. + tpg - 1 of the unit at chunk cw
+                        const int t0 = gw * tpg, t1 = t0 + (tpg > 1 ? 1 : 0);
+                        if (ok) {
+                            if constexpr (GV) {
+                                float ya, yb, yc, yd;
+                                chunk_gemv(st + t0 * kTileRows * rowb, sc + t0 * kTileRows * scb, rowb,
+                                           scb, cw, g, q, bh[0], ya, yb);
+                                chunk_gemv(st + t1 * kTileRows * rowb, sc + t1 * kTileRows * scb, rowb,
+                                           scb, cw, g, q, bh[0], yc, yd);
+                                a0[0] = ya;
+                                a0[2] = yb;
+                                c0[0] = yc;
+                                c0[2] = yd;
+                            } else {
+                                chunk_mma(st + t0 * kTileRows * rowb, sc + t0 * kTileRows * scb, rowb,
+                                          scb, cw, g, q, bh[0], a0, a1);
+                                chunk_mma(st + t1 * kTileRows * rowb, sc + t1 * kTileRows * scb, rowb,
+                                          scb, cw, g, q, bh[0], c0, c1);
+                            }
+                        }
+                    } else if (ok) {
 #pragma unroll
                         for (int m = 0; m < MC_D; ++m) {
                             const int c = warp + kConsumerWarps * m;

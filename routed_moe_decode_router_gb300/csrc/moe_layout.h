@@ -148,6 +148,7 @@ struct LayerParams {
     float rsf;
     int stages;
     uint32_t slot_bytes;
+    int down_rows;          // output rows of a down unit: 32, or 64 (wide units)
     const uint16_t *x;
     uint16_t *out;
     const uint16_t *router_bf16;

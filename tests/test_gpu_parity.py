@@ -50,6 +50,8 @@ SMALL_SHAPES = {
                               norm_topk_prob=False),
     "e300_softmax_no_norm": S(hidden=256, num_experts=300, top_k=5, moe_inter=256,
                               shared_inter=128, norm_topk_prob=False),
+    # 64-row down units with 4-chunk routed and 2-chunk shared intermediates
+    "wide_down_mixed": S(hidden=512, num_experts=32, top_k=8, moe_inter=512, shared_inter=256),
 }
 
 
