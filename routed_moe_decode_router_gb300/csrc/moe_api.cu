@@ -366,6 +366,16 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     auto narrow = [](int inter) { return inter == 2 * kChunk || inter == 4 * kChunk; };
     const bool wide = narrow(cfg->moe_inter) && (!cfg->has_shared || narrow(cfg->shared_inter));
     lp.down_rows = wide ? 2 * kOutTile : kOutTile;
+    // Otherwise, when every entry's intermediate is 8, 12 or 16 chunks, each
+    // compute warp takes one of a unit's two 16-row tiles at a quarter of its
+    // chunks ("split" units): the same work for every warp and four partial
+    // sums a tile for the epilogue.
+    auto quarters = [](int inter) {
+        const int n = inter / kChunk;
+        return n % 4 == 0 && n >= 8 && n <= 16;
+    };
+    lp.down_split = !wide && quarters(cfg->moe_inter) &&
+                    (!cfg->has_shared || quarters(cfg->shared_inter));
     // Ring slot = one 16-row gate or up tile (16 x H/2 packed + 16 x H/16
     // scale bytes) or one down tile (down_rows x I/2 + down_rows x I/16); a
     // gate+up unit takes two slots, a down unit one.
@@ -379,7 +389,8 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
         return fail(MOE_ERR_UNSUPPORTED, "stage ring does not fit in shared memory");
     lp.stages = S;
     const int mc_gu = (cfg->hidden / kChunk + kConsumerWarps - 1) / kConsumerWarps;
-    const int mc_d = (L.inter_max / kChunk + kConsumerWarps - 1) / kConsumerWarps;
+    const int mc_d = lp.down_split ? L.inter_max / kChunk / 4
+                                   : (L.inter_max / kChunk + kConsumerWarps - 1) / kConsumerWarps;
 
     cudaError_t e = cudaSuccess;
     if (ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st);

@@ -164,6 +164,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     // 16-row tiles are spread over all eight compute warps)
     const int DR = p.down_rows, Hd = H / DR;
     const bool wide = DR == 2 * kOutTile;
+    // "split" 32-row units (down_split): warp w multiplies tile w / 4 of the
+    // unit at chunks w % 4 + 4 m, so an intermediate of 8, 12 or 16 chunks
+    // gives every warp the same work and the epilogue four partials a tile
+    const bool split = p.down_split != 0;
     const int Sd = p.has_shared ? Hd : 0;
     const bool is_comp = warp < kConsumerWarps;
     const bool is_epi = warp == kEpiWarp || warp == kEpiWarp2;
@@ -585,6 +589,35 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 }
                 continue;
             }
+            if (split) {
+                // tile `half` from warps 4 * half .. + 3 (chunk groups 0..3)
+                const int o = tile * kOutTile + half * kTileRows + r0;
+                float *dst = (entry == kSharedEntry)
+                                 ? p.ws.ysbuf + (size_t)col * H + o
+                                 : p.ws.ybuf + ((size_t)col * k + (live ? sm.uni.uslot[entry][col] : 0)) * H + o;
+                const int off0 = partial_index(col, r0), off1 = partial_index(col, r0 + 4);
+                ring_wait(&sm.red_full[rb], (ui / kRed) & 1, abort, hdr, 0x200000u + (uint32_t)ui);
+                float4 a[4], c[4];
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    a[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][4 * half + w][off0]);
+                    c[w] = *reinterpret_cast<const float4 *>(&sm.red[rb][4 * half + w][off1]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.red_empty[rb]);
+                float4 u = a[0], v = c[0];
+#pragma unroll
+                for (int w = 1; w < 4; ++w) {
+                    u.x += a[w].x; u.y += a[w].y; u.z += a[w].z; u.w += a[w].w;
+                    v.x += c[w].x; v.y += c[w].y; v.z += c[w].z; v.w += c[w].w;
+                }
+                if (live && !*abort) {
+                    *reinterpret_cast<float4 *>(dst) = make_float4(u.x * s2, u.y * s2, u.z * s2, u.w * s2);
+                    *reinterpret_cast<float4 *>(dst + 4) =
+                        make_float4(v.x * s2, v.y * s2, v.z * s2, v.w * s2);
+                }
+                continue;
+            }
             const int nwd = min(kConsumerWarps, K / kChunk);   // warps holding down partials
             const int o = tile * kOutTile + half * kTileRows + r0;
             float *dst = (entry == kSharedEntry)
@@ -747,12 +780,14 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 const int nch = K / kChunk;
                 const uint32_t rowb = (uint32_t)K / 2, scb = (uint32_t)K / 16;
                 // wide units: this warp's chunk and tile group
-                const int cw = wide ? warp % nch : warp, gw = wide ? warp / nch : 0;
+                // (split units: chunk group warp % 4, tile warp / 4)
+                const int cw = wide ? warp % nch : (split ? warp % 4 : warp);
+                const int gw = wide ? warp / nch : (split ? warp / 4 : 0);
                 const int tpg = nch / 2;
                 MOE_TIC(t_b);
                 load_b<MC_D, GV>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
-                             (size_t)p.ws.inter_max, mask, nch, cw, wide ? nch : kConsumerWarps,
-                             lane, bh, inv0, inv1);
+                             (size_t)p.ws.inter_max, mask, nch, cw,
+                             wide ? nch : (split ? 4 : kConsumerWarps), lane, bh, inv0, inv1);
                 MOE_TOC(tid == 0, 21, t_b);
                 for (; j < jend; ++j) {
                     const int s = rs;
@@ -785,6 +820,26 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                                           scb, cw, g, q, bh[0], a0, a1);
                                 chunk_mma(st + t1 * kTileRows * rowb, sc + t1 * kTileRows * scb, rowb,
                                           scb, cw, g, q, bh[0], c0, c1);
+                            }
+                        }
+                    } else if (split) {
+                        // tile gw of the unit at chunks cw + 4 m
+                        if (ok) {
+#pragma unroll
+                            for (int m = 0; m < MC_D; ++m) {
+                                const int c = cw + 4 * m;
+                                if (c < nch) {
+                                    if constexpr (GV) {
+                                        float ya, yb;
+                                        chunk_gemv(st + gw * kTileRows * rowb, sc + gw * kTileRows * scb,
+                                                   rowb, scb, c, g, q, bh[m], ya, yb);
+                                        a0[0] += ya;
+                                        a0[2] += yb;
+                                    } else {
+                                        chunk_mma(st + gw * kTileRows * rowb, sc + gw * kTileRows * scb,
+                                                  rowb, scb, c, g, q, bh[m], a0, a1);
+                                    }
+                                }
                             }
                         }
                     } else if (ok) {

@@ -149,6 +149,7 @@ struct LayerParams {
     int stages;
     uint32_t slot_bytes;
     int down_rows;          // output rows of a down unit: 32, or 64 (wide units)
+    int down_split;         // 32-row units whose 8, 12 or 16 chunks go four to a tile
     const uint16_t *x;
     uint16_t *out;
     const uint16_t *router_bf16;

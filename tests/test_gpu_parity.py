@@ -52,6 +52,8 @@ SMALL_SHAPES = {
                               shared_inter=128, norm_topk_prob=False),
     # 64-row down units with 4-chunk routed and 2-chunk shared intermediates
     "wide_down_mixed": S(hidden=512, num_experts=32, top_k=8, moe_inter=512, shared_inter=256),
+    # 32-row down units split four chunk groups to a tile (8 and 16 chunks)
+    "split_down_mixed": S(hidden=512, num_experts=16, top_k=4, moe_inter=1024, shared_inter=2048),
 }
 
 
