@@ -288,7 +288,7 @@ void orc_route(const orc_cfg *c, const orc_weights *w, const uint16_t *x,
  * uni[U], slot2u[rows][k] (union index of every (row, slot)) and rowmask[U]
  * (bit r set when row r selected uni[u]). */
 int orc_union(const int32_t *ids, int rows, int k, int32_t *uni,
-              uint8_t *slot2u, uint8_t *rowmask)
+              uint8_t *slot2u, uint32_t *rowmask)
 {
     int U = 0;
     for (int p = 0; p < rows * k; ++p) {
@@ -305,7 +305,7 @@ int orc_union(const int32_t *ids, int rows, int k, int32_t *uni,
             ++U;
         }
         slot2u[p] = (uint8_t)found;
-        rowmask[found] |= (uint8_t)(1u << (p / k));
+        rowmask[found] |= (uint32_t)(1u << (p / k));
     }
     return U;
 }

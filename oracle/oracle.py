@@ -176,7 +176,8 @@ def union(ids: np.ndarray):
     rows, k = ids.shape
     uni = np.zeros(rows * k, dtype=np.int32)
     slot2u = np.zeros((rows, k), dtype=np.uint8)
-    rowmask = np.zeros(rows * k, dtype=np.uint8)
+    assert rows <= 32, "row masks are 32 bits wide"
+    rowmask = np.zeros(rows * k, dtype=np.uint32)
     U = lib().orc_union(_ptr(ids), rows, k, _ptr(uni), _ptr(slot2u),
                         _ptr(rowmask))
     return U, uni[:U].copy(), slot2u, rowmask[:U].copy()

@@ -339,12 +339,29 @@ def test_union_vs_python_first_occurrence(orc):
             assert U == k
 
 
+def test_union_of_32_rows_vs_python_first_occurrence(orc):
+    """Prefill chunks wider than one 8-row sub-chunk: the union of up to 32
+    rows (256 ids) is the same first-occurrence scan, with 32-bit row masks."""
+    rng = np.random.default_rng(13)
+    for rows, k, E in ((32, 8, 160), (16, 8, 512), (24, 4, 40), (32, 2, 7)):
+        ids = np.stack([rng.choice(E, size=k, replace=False) for _ in range(rows)])
+        U, uni, slot2u, rowmask = orc.union(ids)
+        first = list(dict.fromkeys(int(v) for v in ids.ravel()))
+        assert U == len(first) and [int(v) for v in uni] == first
+        for u, e in enumerate(first):
+            rows_with = {r for r in range(rows) if e in ids[r]}
+            assert {r for r in range(32) if int(rowmask[u]) >> r & 1} == rows_with
+        for r in range(rows):
+            for j in range(k):
+                assert first[slot2u[r, j]] == ids[r, j]
+
+
 def test_union_ignores_prior_buffer_contents(orc):
     """The union fills its output arrays whatever they held before."""
     ids = np.array([[3, 1], [1, 4]], dtype=np.int32)
     uni = np.full(4, -7, dtype=np.int32)
     slot2u = np.full((2, 2), 0xEE, dtype=np.uint8)
-    rowmask = np.full(4, 0xFF, dtype=np.uint8)
+    rowmask = np.full(4, 0xFF, dtype=np.uint32)
     U = orc.lib().orc_union(ids.ctypes.data, 2, 2, uni.ctypes.data, slot2u.ctypes.data,
                             rowmask.ctypes.data)
     assert U == 3 and list(uni[:3]) == [3, 1, 4]
