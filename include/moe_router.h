@@ -59,8 +59,12 @@ extern "C" {
 #endif
 
 #define MOE_ABI_VERSION 2
-#define MOE_MAX_ROWS 8        /* rows per call (forward_moe page, WIDENED note) */
-#define MOE_MAX_IDS 64        /* rows * top_k: one block's pairwise scan */
+#define MOE_MAX_ROWS 32       /* rows per call */
+#define MOE_MAX_IDS 256       /* rows * top_k per call (the union's capacity) */
+#define MOE_CHUNK_ROWS 8      /* rows per sub-chunk of the expert sweep ... */
+#define MOE_CHUNK_IDS 64      /* ... whose union of at most 64 ids fits one
+                                 block's pairwise scan (forward_moe page,
+                                 WIDENED note: 8 * 8 == 64) */
 #define MOE_MAX_HIDDEN 4096
 #define MOE_MAX_EXPERTS 1024
 
@@ -155,15 +159,16 @@ typedef struct moe_weights {
     const uint16_t *shared_expert_gate; /* device [H] bf16 (shared_gate = 1) */
 } moe_weights;
 
-/* Result of the union step (device-resident; moe_union and
- * moe_read_routing copy it out).  Positions p = row * top_k + slot. */
+/* Union of the experts selected by all rows of a call (device-resident;
+ * moe_union and moe_read_routing copy it out): the first occurrences of the
+ * ids in row-major (row, slot) order.  Positions p = row * top_k + slot. */
 typedef struct moe_union_table {
     int32_t num_union;                  /* U <= min(rows * top_k, E) */
     int32_t rows;
     int32_t top_k;
     int32_t per_row_mode;
     int32_t expert[MOE_MAX_IDS];        /* union[u]: expert id, u < U */
-    uint8_t rowmask[MOE_MAX_IDS];       /* bit r: row r selected union[u] */
+    uint32_t rowmask[MOE_MAX_IDS];      /* bit r: row r selected union[u] */
     uint8_t slot2u[MOE_MAX_IDS];        /* [p]: union index of position p */
     uint8_t uslot[MOE_MAX_IDS][MOE_MAX_ROWS]; /* [u][r]: slot of union[u] in
                                            row r, 0xFF if r did not pick it */
@@ -195,8 +200,9 @@ MOE_API size_t moe_workspace_size(const moe_config *cfg);
  * change of row count or timed-out launch needs a second initialisation. */
 MOE_API moe_status moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
-/* Router + top-k for `rows` rows (forward_token_major.rs: gate projection
- * then moe_topk_softmax_batched / moe_topk_sigmoid_batched).
+/* Router + top-k for `rows` rows, 1..MOE_MAX_ROWS with rows * top_k <=
+ * MOE_MAX_IDS (forward_token_major.rs: gate projection then
+ * moe_topk_softmax_batched / moe_topk_sigmoid_batched).
  *   x       device [rows][H] bf16, 16-byte aligned
  *   ids     device [rows][top_k] int32, descending score, ties -> lower id
  *   wts     device [rows][top_k] fp32 routing weights
@@ -205,18 +211,22 @@ MOE_API moe_status moe_route(const moe_config *cfg, const moe_weights *w,
                      const uint16_t *x, int rows, int32_t *ids, float *wts,
                      float *logits, void *ws, size_t ws_bytes, void *stream);
 
-/* Union of caller-given ids [rows][top_k] (device int32) by one block's
- * pairwise scan (forward_moe page, RETRACTED note), with the device pointer
- * table of the union experts built in the workspace.  `out` is a device
- * moe_union_table.  `w` supplies the expert tables for the pointer table
- * and may be NULL (no pointer table).  Ids outside [0, E) are recorded as
- * MOE_DEV_BAD_EXPERT_ID and skipped. */
+/* Union of caller-given ids [rows][top_k] (device int32, rows * top_k <=
+ * MOE_MAX_IDS) by pairwise scan (forward_moe page, RETRACTED note: no
+ * sort), with the device pointer table of the union experts built in the
+ * workspace.  The ids are scanned in blocks of MOE_CHUNK_IDS: a position
+ * opens a union entry when no earlier position, in its own block or an
+ * earlier one, holds the same id, so the entries keep first-occurrence
+ * order across blocks.  `out` is a device moe_union_table.  `w` supplies
+ * the expert tables for the pointer table and may be NULL (no pointer
+ * table).  Ids outside [0, E) are recorded as MOE_DEV_BAD_EXPERT_ID and
+ * skipped. */
 MOE_API moe_status moe_union(const moe_config *cfg, const moe_weights *w,
                      const int32_t *ids, int rows, moe_union_table *out,
                      void *ws, size_t ws_bytes, void *stream);
 
 /* The whole routed MoE layer (page "Function forward_moe": forward_moe(x,
- * out, rows)):
+ * out, rows)) for rows = 1..MOE_MAX_ROWS with rows * top_k <= MOE_MAX_IDS:
  *   out[r] = sum_{slot < k} wts[r][slot] * Expert_{ids[r][slot]}(x[r])
  *            + g_r * Shared(x[r]),
  *   Expert(x) = Wd (silu(Wg x) * (Wu x)), g_r = sigmoid(x[r] . gs) with
@@ -224,7 +234,14 @@ MOE_API moe_status moe_union(const moe_config *cfg, const moe_weights *w,
  *   x    device [rows][H] bf16, 16-byte aligned
  *   out  device [rows][H] bf16, 16-byte aligned, must not overlap x
  * `out` is the MoE output only (the residual add is the caller's).  Nothing
- * is read back to the host, so the call can be captured in a CUDA graph. */
+ * is read back to the host, so the call can be captured in a CUDA graph.
+ * Rows are taken in consecutive sub-chunks of min(MOE_CHUNK_ROWS,
+ * MOE_CHUNK_IDS / top_k) rows, one kernel launch each, as the page batches
+ * prefill in 8-row sub-chunks: a sub-chunk's union (at most MOE_CHUNK_IDS
+ * ids, one block) is swept once for all its rows, and every row's output
+ * bytes are those a call with that sub-chunk alone would give.  A call of
+ * more than one sub-chunk then resolves the union of all its rows (as
+ * moe_union does) for moe_read_routing. */
 MOE_API moe_status moe_forward(const moe_config *cfg, const moe_weights *w,
                        const uint16_t *x, uint16_t *out, int rows, void *ws,
                        size_t ws_bytes, void *stream);
@@ -269,7 +286,8 @@ MOE_API moe_status moe_forward_static(const moe_config *cfg, const moe_weights *
 /* Copy the routing of the last moe_forward / moe_route on this workspace
  * into caller buffers (async device-to-device copies on `stream`; any
  * pointer may be NULL): ids / wts device [rows][top_k], uni a device
- * moe_union_table (valid after moe_forward or moe_union). */
+ * moe_union_table of all the call's rows (valid after moe_forward or
+ * moe_union). */
 MOE_API moe_status moe_read_routing(const moe_config *cfg, const void *ws,
                             size_t ws_bytes, int rows, int32_t *ids,
                             float *wts, moe_union_table *uni, void *stream);

@@ -85,9 +85,9 @@ moe_status check_cfg(const moe_config *c) {
                     "router_width=%d differs from num_experts=%d: zero-computation experts "
                     "are not supported by this path",
                     c->router_width, c->num_experts);
-    if (c->top_k < 1 || c->top_k > c->num_experts || c->top_k > MOE_MAX_IDS)
+    if (c->top_k < 1 || c->top_k > c->num_experts || c->top_k > MOE_CHUNK_IDS)
         return fail(MOE_ERR_INVALID_ARG, "top_k=%d: must be in [1, min(num_experts, %d)]",
-                    c->top_k, MOE_MAX_IDS);
+                    c->top_k, MOE_CHUNK_IDS);
     if (c->moe_inter < kChunk || c->moe_inter % kChunk || c->moe_inter > 4 * kConsumerWarps * kChunk)
         return fail(MOE_ERR_INVALID_ARG, "moe_inter=%d: must be a multiple of %d in [%d, %d]",
                     c->moe_inter, kChunk, kChunk, 4 * kConsumerWarps * kChunk);
@@ -121,10 +121,38 @@ moe_status check_rows(const moe_config *c, int rows) {
     if (rows < 1 || rows > MOE_MAX_ROWS)
         return fail(MOE_ERR_INVALID_ARG, "rows=%d: must be in [1, %d]", rows, MOE_MAX_ROWS);
     if (rows * c->top_k > MOE_MAX_IDS)
-        return fail(MOE_ERR_UNSUPPORTED,
-                    "rows*top_k=%d exceeds %d ids (one block's pairwise scan)",
+        return fail(MOE_ERR_UNSUPPORTED, "rows*top_k=%d exceeds %d ids (the union's capacity)",
                     rows * c->top_k, MOE_MAX_IDS);
     return MOE_OK;
+}
+
+// Rows of one sub-chunk: at most 8, and at most 64 ids (one union block).
+int chunk_rows(const moe_config *c) {
+    const int r = MOE_CHUNK_IDS / c->top_k;
+    return r < MOE_CHUNK_ROWS ? r : MOE_CHUNK_ROWS;
+}
+
+UnionParams union_params(const moe_config *c, const moe_weights *w, const int32_t *ids, int rows,
+                         const WsPtrs &wp, moe_union_table *out) {
+    UnionParams p{};
+    p.E = c->num_experts;
+    p.k = c->top_k;
+    p.rows = rows;
+    p.per_row_mode = c->per_row_mode;
+    p.has_tables = w != nullptr;
+    p.has_shared = c->has_shared;
+    p.ids = ids;
+    if (w) {
+        p.gate = w->gate;
+        p.up = w->up;
+        p.down = w->down;
+        p.sh_gate = w->shared_gate_proj;
+        p.sh_up = w->shared_up_proj;
+        p.sh_down = w->shared_down_proj;
+    }
+    p.ws = wp;
+    p.out = out;
+    return p;
 }
 
 moe_status check_ws(const moe_config *c, const void *ws, size_t ws_bytes, WsLayout *L) {
@@ -274,13 +302,18 @@ moe_status moe_route(const moe_config *cfg, const moe_weights *w, const uint16_t
         return s;
     if ((ids && !aligned(ids, 4)) || (wts && !aligned(wts, 4)) || (logits && !aligned(logits, 4)))
         return fail(MOE_ERR_INVALID_ARG, "ids / wts / logits must be 4-byte aligned");
-    RouteParams p = route_params(cfg, w, x, rows, ws_ptrs(ws, L));
-    p.do_union = 0;
-    p.ids_out = ids;
-    p.wts_out = wts;
-    p.logits_out = logits;
-    cudaError_t e = launch_route(p, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+    // one launch per sub-chunk of at most 8 rows
+    const int cr = chunk_rows(cfg), H = cfg->hidden, E = cfg->num_experts, k = cfg->top_k;
+    for (int r0 = 0; r0 < rows; r0 += cr) {
+        const int n = rows - r0 < cr ? rows - r0 : cr;
+        RouteParams p = route_params(cfg, w, x + (size_t)r0 * H, n, ws_ptrs(ws, L));
+        p.row_base = r0;
+        p.ids_out = ids ? ids + (size_t)r0 * k : nullptr;
+        p.wts_out = wts ? wts + (size_t)r0 * k : nullptr;
+        p.logits_out = logits ? logits + (size_t)r0 * E : nullptr;
+        cudaError_t e = launch_route(p, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+    }
     return ok();
 }
 
@@ -294,24 +327,7 @@ moe_status moe_union(const moe_config *cfg, const moe_weights *w, const int32_t 
     if (!ids || !aligned(ids, 4)) return fail(MOE_ERR_INVALID_ARG, "ids: NULL or misaligned");
     if (out && !aligned(out, 4)) return fail(MOE_ERR_INVALID_ARG, "out: misaligned");
     if (w && (s = check_weights(cfg, w, true)) != MOE_OK) return s;
-    UnionParams p{};
-    p.E = cfg->num_experts;
-    p.k = cfg->top_k;
-    p.rows = rows;
-    p.per_row_mode = cfg->per_row_mode;
-    p.has_tables = w != nullptr;
-    p.has_shared = cfg->has_shared;
-    p.ids = ids;
-    if (w) {
-        p.gate = w->gate;
-        p.up = w->up;
-        p.down = w->down;
-        p.sh_gate = w->shared_gate_proj;
-        p.sh_up = w->shared_up_proj;
-        p.sh_down = w->shared_down_proj;
-    }
-    p.ws = ws_ptrs(ws, L);
-    p.out = out;
+    const UnionParams p = union_params(cfg, w, ids, rows, ws_ptrs(ws, L), out);
     cudaError_t e = launch_union(p, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "union launch: %s", cudaGetErrorString(e));
     return ok();
@@ -392,11 +408,24 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     const int mc_d = lp.down_split ? L.inter_max / kChunk / 4
                                    : (L.inter_max / kChunk + kConsumerWarps - 1) / kConsumerWarps;
 
+    // one launch per sub-chunk of at most 8 rows (64 ids), in row order; a
+    // call of several sub-chunks then resolves the union of all its rows
+    const int cr = chunk_rows(cfg), H = cfg->hidden;
+    const int nchunks = (rows + cr - 1) / cr;
     cudaError_t e = cudaSuccess;
     if (ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st);
-    if (e == cudaSuccess)
+    for (int c = 0; c < nchunks && e == cudaSuccess; ++c) {
+        const int r0 = c * cr, n = rows - r0 < cr ? rows - r0 : cr;
+        lp.rows = n;
+        lp.row_base = r0;
+        lp.publish_union = nchunks == 1;
+        lp.x = x + (size_t)r0 * H;
+        lp.out = out + (size_t)r0 * H;
         e = launch_layer(lp, di->sms, layer_smem_bytes(S, lp.slot_bytes), mc_gu, mc_d,
                          rows == 1 && cfg->gemv_lever, st);
+    }
+    if (e == cudaSuccess && nchunks > 1)
+        e = launch_union(union_params(cfg, w, lp.ws.ids, rows, lp.ws, nullptr), st);
     if (e == cudaSuccess && ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[1]), st);
     if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "layer launch: %s", cudaGetErrorString(e));
     return ok();

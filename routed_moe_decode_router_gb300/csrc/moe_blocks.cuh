@@ -211,8 +211,9 @@ struct UnionSrc {
     moe_nvfp4 sh_gate, sh_up, sh_down;
 };
 
-// Union of the rows * k ids in s_ids (position p = row * k + slot) by
-// pairwise scan (page "Function forward_moe", RETRACTED note): position p
+// Union of the rows * k <= 64 ids of one sub-chunk in s_ids (position p =
+// row * k + slot) by pairwise scan (page "Function forward_moe", RETRACTED
+// note): position p
 // opens a union entry when no earlier position holds the same id; entries
 // keep first-occurrence order; no sort.  Lane l holds positions l and l + 32;
 // the comparisons against earlier positions run on registers (warp match
@@ -222,7 +223,7 @@ struct UnionSrc {
 // s_mask is 64 words of scratch shared memory.  All 32 lanes of one warp
 // call it.
 __device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, uint32_t *s_mask,
-                                   moe_union_table *ut, PtrEntry *ptrs, WsHeader *hdr, int lane) {
+                                   ChunkUnion *ut, PtrEntry *ptrs, WsHeader *hdr, int lane) {
     const unsigned FULL = 0xffffffffu;
     const int n = src.rows * src.k;
     const int p0 = lane, p1 = lane + 32;

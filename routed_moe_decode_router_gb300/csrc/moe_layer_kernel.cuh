@@ -89,7 +89,7 @@ static_assert(kRed == kEpiWarps, "each epilogue warp owns one partial-sum buffer
 struct LayerSmem {
     float red[kRed][kConsumerWarps][256];       // compute warps' partial sums
     float rpart[kRouterRowsPerPass][kMaxSegs][kMaxRows];   // router partial dots
-    moe_union_table uni;
+    ChunkUnion uni;
     PtrEntry ptrs[kEntries];
     int32_t ids[kMaxIds];
     float wts[kMaxIds];
@@ -391,12 +391,30 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         if (b == 0) {   // publish the routing for moe_read_routing
             const int n = p.rows * k;
             for (int i = lane; i < n; i += 32) {
-                p.ws.ids[i] = sm.ids[i];
-                p.ws.wts[i] = sm.wts[i];
+                p.ws.ids[p.row_base * k + i] = sm.ids[i];
+                p.ws.wts[p.row_base * k + i] = sm.wts[i];
             }
-            const uint32_t *su = reinterpret_cast<const uint32_t *>(&sm.uni);
-            uint32_t *du = reinterpret_cast<uint32_t *>(p.ws.uni);
-            for (int i = lane; i < (int)(sizeof(moe_union_table) / 4); i += 32) du[i] = su[i];
+            if (p.publish_union) {   // this sub-chunk is the whole call
+                moe_union_table *g = p.ws.uni;
+                uint4 *us = reinterpret_cast<uint4 *>(&g->uslot[0][0]);
+                for (int i = lane; i < (int)(sizeof(g->uslot) / 16); i += 32)
+                    us[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+                __syncwarp();
+                const int U = sm.uni.num_union;
+                for (int u = lane; u < U; u += 32) {
+                    g->expert[u] = sm.uni.expert[u];
+                    g->rowmask[u] = sm.uni.rowmask[u];
+#pragma unroll
+                    for (int r = 0; r < kMaxRows; ++r) g->uslot[u][r] = sm.uni.uslot[u][r];
+                }
+                for (int i = lane; i < n; i += 32) g->slot2u[i] = sm.uni.slot2u[i];
+                if (lane == 0) {
+                    g->num_union = U;
+                    g->rows = p.rows;
+                    g->top_k = k;
+                    g->per_row_mode = p.per_row_mode;
+                }
+            }
             if (lane < kMaxRows && !gate_row) p.ws.gate_val[lane] = sm.gate_val[lane];
         }
     } else if (is_prod || warp == kEpiWarp2) {

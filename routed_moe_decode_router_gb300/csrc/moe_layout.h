@@ -9,10 +9,27 @@
 
 namespace moe {
 
-constexpr int kMaxRows = MOE_MAX_ROWS;
-constexpr int kMaxIds = MOE_MAX_IDS;
+// One pass of the layer kernel: a sub-chunk of at most 8 rows and 64 ids.
+constexpr int kMaxRows = MOE_CHUNK_ROWS;
+constexpr int kMaxIds = MOE_CHUNK_IDS;
 constexpr int kSharedEntry = kMaxIds;    // pointer-table slot of the shared expert
 constexpr int kEntries = kMaxIds + 1;
+// One call: up to 32 rows and 256 ids (several sub-chunks).
+constexpr int kCallRows = MOE_MAX_ROWS;
+constexpr int kCallIds = MOE_MAX_IDS;
+
+// The union of one sub-chunk, as the layer kernel keeps it in shared memory
+// (positions p = row * top_k + slot of the sub-chunk).
+struct ChunkUnion {
+    int32_t num_union;
+    int32_t rows;
+    int32_t top_k;
+    int32_t per_row_mode;
+    int32_t expert[kMaxIds];
+    uint8_t rowmask[kMaxIds];
+    uint8_t slot2u[kMaxIds];
+    uint8_t uslot[kMaxIds][kMaxRows];
+};
 constexpr int kTileRows = 16;            // output rows of one MMA tile (M)
 constexpr int kOutTile = 32;             // output rows of a down unit / blend tile
 constexpr int kChunk = 128;              // inputs per compute-warp chunk
@@ -53,8 +70,11 @@ static_assert(sizeof(PtrEntry) == 64, "pointer entry size");
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Byte offsets of every workspace region for one configuration.  The layout
-// is sized for MOE_MAX_ROWS rows, so one workspace serves every row count.
+// Byte offsets of every workspace region for one configuration.  The ids,
+// weights, union table and pointer table are sized for a whole call (32
+// rows, 256 ids); the logits and the intermediate activations for one
+// sub-chunk (8 rows), which the sub-chunks of a call reuse in turn.  One
+// workspace serves every row count.
 struct WsLayout {
     size_t header, ids, wts, logits, gate_val, uni, ptrs, hbuf, ybuf, ysbuf, total;
     int inter_max;          // max(I, Is): row stride of the h buffer
@@ -64,12 +84,12 @@ struct WsLayout {
         size_t o = 0;
         L.header = o;   o = align256(o + sizeof(WsHeader));
         // forward_token_major.rs scratch order: ids, then routing weights.
-        L.ids = o;      o += sizeof(int32_t) * (size_t)kMaxIds;
-        L.wts = o;      o = align256(o + sizeof(float) * (size_t)kMaxIds);
+        L.ids = o;      o += sizeof(int32_t) * (size_t)kCallIds;
+        L.wts = o;      o = align256(o + sizeof(float) * (size_t)kCallIds);
         L.logits = o;   o = align256(o + sizeof(float) * (size_t)kMaxRows * c.num_experts);
         L.gate_val = o; o = align256(o + sizeof(float) * kMaxRows);
         L.uni = o;      o = align256(o + sizeof(moe_union_table));
-        L.ptrs = o;     o = align256(o + sizeof(PtrEntry) * kEntries);
+        L.ptrs = o;     o = align256(o + sizeof(PtrEntry) * (kCallIds + 1));
         L.inter_max = c.moe_inter;
         if (c.has_shared && c.shared_inter > L.inter_max) L.inter_max = c.shared_inter;
         L.hbuf = o;     o = align256(o + 2 * (size_t)kEntries * kMaxRows * L.inter_max);
@@ -87,8 +107,8 @@ struct WsPtrs {
     float *wts;
     float *logits;
     float *gate_val;
-    moe_union_table *uni;
-    PtrEntry *ptrs;
+    moe_union_table *uni;   // the call's union (all its rows)
+    PtrEntry *ptrs;         // [kCallIds + 1]: union entries, the shared expert last
     uint16_t *hbuf;   // bf16 [kEntries][kMaxRows][inter_max]
     float *ybuf;      // fp32 [kMaxIds][H]: position p = row * top_k + slot
     float *ysbuf;     // fp32 [kMaxRows][H]: shared expert output
@@ -112,11 +132,11 @@ inline WsPtrs ws_ptrs(void *ws, const WsLayout &L) {
     return p;
 }
 
-// Parameters of the route kernel (router + top-k [+ union]).
+// Parameters of the route kernel (router + top-k) for one sub-chunk of at
+// most 8 rows, the call's rows row_base .. row_base + rows - 1.
 struct RouteParams {
-    int H, E, k, rows;
+    int H, E, k, rows, row_base;
     int scoring, norm, router_fmt, has_shared, shared_gated, per_row_mode;
-    int do_union;
     float rsf;
     const uint16_t *x;
     const uint16_t *router_bf16;
@@ -131,7 +151,8 @@ struct RouteParams {
     float *logits_out;
 };
 
-// Parameters of the union-only kernel (moe_union).
+// Parameters of the union kernel (moe_union, and calls of several
+// sub-chunks): up to kCallIds ids.
 struct UnionParams {
     int E, k, rows, per_row_mode, has_tables, has_shared;
     const int32_t *ids;
@@ -141,9 +162,13 @@ struct UnionParams {
     moe_union_table *out;
 };
 
-// Parameters of the persistent layer kernel.
+// Parameters of the persistent layer kernel for one sub-chunk of at most 8
+// rows, the call's rows row_base .. row_base + rows - 1.  publish_union: the
+// call has only this sub-chunk, so its union is the call's (written to the
+// workspace for moe_read_routing).
 struct LayerParams {
     int H, E, k, rows, I, Is;
+    int row_base, publish_union;
     int scoring, norm, router_fmt, has_shared, shared_gated, per_row_mode;
     float rsf;
     int stages;

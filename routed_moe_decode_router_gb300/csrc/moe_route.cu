@@ -11,15 +11,19 @@
 // moe_topk_sigmoid_batched; forward_ep.rs: moe_topk_softmax) runs in the
 // block that finishes last (an atomic ticket), one warp per token row:
 // selection key descending with ties to the lower expert id; softmax selects
-// on the logit, sigmoid scoring on sigmoid(logit) + correction bias.
+// on the logit, sigmoid scoring on sigmoid(logit) + correction bias.  One
+// launch covers a sub-chunk of at most 8 rows; a call of more rows launches
+// one per sub-chunk.
 //
-// Union (page "Function forward_moe", RETRACTED and WIDENED notes): the
-// (at most 64) ids of all rows are de-duplicated by one warp -- a position
-// starts a union entry when no earlier position holds the same id -- with no
-// sort and no copy to the host.  The same warp writes the device pointer
-// table of the union experts (the forward_moe page's pointer-table upgrade
-// path) into the workspace, for inspection through moe_union; the layer
-// kernel builds its own copy of the table in shared memory.
+// Union (page "Function forward_moe", RETRACTED and WIDENED notes): the ids
+// of all the call's rows (at most 256) are de-duplicated by pairwise scan in
+// blocks of 64 -- a position starts a union entry when no earlier position,
+// in its own block or an earlier one, holds the same id -- with no sort and
+// no copy to the host.  The kernel writes the call's union table and the
+// device pointer table of the union experts (the forward_moe page's
+// pointer-table upgrade path) into the workspace, for moe_union and for
+// calls of several sub-chunks; the layer kernel builds its own copy of a
+// sub-chunk's table in shared memory.
 #include <cuda_runtime.h>
 
 #include "moe_blocks.cuh"
@@ -120,7 +124,6 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     moe_route_kernel(const RouteParams p) {
     __shared__ int32_t s_ids[kMaxIds];
     __shared__ float s_wts[kMaxIds];
-    __shared__ uint32_t s_mask[kMaxIds];
     __shared__ int s_last;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -201,44 +204,117 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
         for (int j = lane; j < k; j += 32) {
             const int id = s_ids[r * k + j];
             const float w = s_wts[r * k + j];
-            p.ws.ids[r * k + j] = id;
-            p.ws.wts[r * k + j] = w;
+            p.ws.ids[(p.row_base + r) * k + j] = id;
+            p.ws.wts[(p.row_base + r) * k + j] = w;
             if (p.ids_out) p.ids_out[r * k + j] = id;
             if (p.wts_out) p.wts_out[r * k + j] = w;
         }
     }
     if (threadIdx.x < kMaxRows && !(p.has_shared && p.shared_gated))
         p.ws.gate_val[threadIdx.x] = p.has_shared ? 1.f : 0.f;
-    __syncthreads();
-    if (p.do_union && warp == 0) {
-        UnionSrc src{E,      k,      p.rows, p.per_row_mode, 1,        p.has_shared,
-                     p.gate, p.up,   p.down, p.sh_gate,      p.sh_up, p.sh_down};
-        build_union(src, s_ids, s_mask, p.ws.uni, p.ws.ptrs, p.ws.hdr, lane);
-    }
     if (threadIdx.x == 0) p.ws.hdr->route_ticket = 0u;
 }
 
 // ---------------------------------------------------------------------------
-// Union-only kernel (one warp)
+// Union kernel: up to kCallIds ids, one thread per position
 // ---------------------------------------------------------------------------
 
-__global__ void __launch_bounds__(32) moe_union_kernel(const UnionParams p) {
-    __shared__ int32_t s_ids[kMaxIds];
-    __shared__ uint32_t s_mask[kMaxIds];
-    const int lane = threadIdx.x;
+__global__ void __launch_bounds__(kCallIds) moe_union_kernel(const UnionParams p) {
+    __shared__ int32_t s_ids[kCallIds];
+    __shared__ int s_uidx[kCallIds];              // union index of each first occurrence
+    __shared__ int s_wfirst[kCallIds / 32];       // first occurrences per warp
+    __shared__ uint32_t s_mask[kCallIds];         // row mask of each union entry
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int k = p.k, n = p.rows * k;
     pdl_wait();
-    const int n = p.rows * p.k;
-    for (int i = lane; i < kMaxIds; i += 32) s_ids[i] = i < n ? p.ids[i] : -1;
-    __syncwarp();
-    UnionSrc src{p.E,    p.k,    p.rows, p.per_row_mode, p.has_tables, p.has_shared,
-                 p.gate, p.up,   p.down, p.sh_gate,      p.sh_up,      p.sh_down};
-    build_union(src, s_ids, s_mask, p.ws.uni, p.ws.ptrs, p.ws.hdr, lane);
-    __syncwarp();
-    if (p.out) {
-        const uint32_t *s = reinterpret_cast<const uint32_t *>(p.ws.uni);
+    // unused positions get distinct negative ids, so they never match
+    const int id = t < n ? p.ids[t] : -1 - t;
+    s_ids[t] = id;
+    s_mask[t] = 0u;
+    __syncthreads();
+    // Pairwise scan in blocks of 64: the earliest position holding this id
+    // (earlier blocks first, then this position's own block); per-row mode
+    // keeps every position.
+    int fq = t;
+    if (!p.per_row_mode && t < n) {
+        const int blk0 = (t / kMaxIds) * kMaxIds;
+        for (int q = 0; q < blk0 && fq == t; ++q)
+            if (s_ids[q] == id) fq = q;
+        for (int q = blk0; q < t && fq == t; ++q)
+            if (s_ids[q] == id) fq = q;
+    }
+    const bool first = t < n && fq == t;
+    const unsigned bal = __ballot_sync(0xffffffffu, first);
+    if (lane == 0) s_wfirst[warp] = __popc(bal);
+    __syncthreads();
+    int base = 0, U = 0;
+#pragma unroll
+    for (int w = 0; w < kCallIds / 32; ++w) {
+        base += w < warp ? s_wfirst[w] : 0;
+        U += s_wfirst[w];
+    }
+    if (first) s_uidx[t] = base + __popc(bal & ((1u << lane) - 1u));
+    moe_union_table *ut = p.ws.uni;
+    uint4 *us = reinterpret_cast<uint4 *>(&ut->uslot[0][0]);
+    for (int i = t; i < (int)(sizeof(ut->uslot) / 16); i += kCallIds)
+        us[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+    __syncthreads();
+    if (t < n) {
+        const int u = s_uidx[fq];
+        ut->slot2u[t] = (uint8_t)u;
+        ut->uslot[u][t / k] = (uint8_t)(t % k);
+        atomicOr(&s_mask[u], 1u << (t / k));
+    }
+    __syncthreads();
+    if (first) {
+        const int u = s_uidx[t];
+        ut->expert[u] = id;
+        ut->rowmask[u] = s_mask[u];
+        if (p.has_tables) {
+            PtrEntry e;
+            if (id < 0 || id >= p.E) {
+                record_fault(p.ws.hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)t);
+                e = PtrEntry{};
+                e.expert = -1;
+            } else {
+                const moe_expert_table tb[3] = {p.gate, p.up, p.down};
+                load_ptr_entry(tb, id, e);
+                bool ok = true;
+#pragma unroll
+                for (int m = 0; m < 3; ++m) ok = ok && aligned16(e.packed[m]) && aligned16(e.scales[m]);
+                if (!ok) {
+                    record_fault(p.ws.hdr, MOE_DEV_MISALIGNED_PTR, (uint32_t)id);
+                    e.expert = -1;
+                }
+            }
+            p.ws.ptrs[u] = e;
+        } else if (id < 0 || id >= p.E) {
+            record_fault(p.ws.hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)t);
+        }
+    }
+    if (t == 0) {
+        ut->num_union = U;
+        ut->rows = p.rows;
+        ut->top_k = k;
+        ut->per_row_mode = p.per_row_mode;
+        if (p.has_tables && p.has_shared) {
+            PtrEntry e;
+            const moe_nvfp4 *sm3[3] = {&p.sh_gate, &p.sh_up, &p.sh_down};
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                e.packed[m] = sm3[m]->packed;
+                e.scales[m] = sm3[m]->scales;
+                e.scale2[m] = sm3[m]->scale2;
+            }
+            e.expert = kSharedEntry;
+            p.ws.ptrs[kCallIds] = e;
+        }
+    }
+    if (p.out) {   // the caller's copy of the table
+        __syncthreads();
+        const uint32_t *s = reinterpret_cast<const uint32_t *>(ut);
         uint32_t *d = reinterpret_cast<uint32_t *>(p.out);
-        __threadfence_block();
-        for (int i = lane; i < (int)(sizeof(moe_union_table) / 4); i += 32) d[i] = s[i];
+        for (int i = t; i < (int)(sizeof(moe_union_table) / 4); i += kCallIds) d[i] = s[i];
     }
 }
 
@@ -269,7 +345,7 @@ cudaError_t launch_route(const RouteParams &p, cudaStream_t stream) {
 cudaError_t launch_union(const UnionParams &p, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(1);
-    cfg.blockDim = dim3(32);
+    cfg.blockDim = dim3(kCallIds);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1] = {pdl_attr()};
     cfg.attrs = attr;

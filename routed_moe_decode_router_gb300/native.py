@@ -13,8 +13,10 @@ import threading
 
 from . import build as _build
 
-MOE_MAX_ROWS = 8
-MOE_MAX_IDS = 64
+MOE_MAX_ROWS = 32
+MOE_MAX_IDS = 256
+MOE_CHUNK_ROWS = 8
+MOE_CHUNK_IDS = 64
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 MOE_ROUTER_BF16, MOE_ROUTER_NVFP4 = 0, 1
 
@@ -63,7 +65,7 @@ class UnionTable(C.Structure):
     _fields_ = [("num_union", C.c_int32), ("rows", C.c_int32),
                 ("top_k", C.c_int32), ("per_row_mode", C.c_int32),
                 ("expert", C.c_int32 * MOE_MAX_IDS),
-                ("rowmask", C.c_uint8 * MOE_MAX_IDS),
+                ("rowmask", C.c_uint32 * MOE_MAX_IDS),
                 ("slot2u", C.c_uint8 * MOE_MAX_IDS),
                 ("uslot", (C.c_uint8 * MOE_MAX_ROWS) * MOE_MAX_IDS)]
 

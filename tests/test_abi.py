@@ -98,6 +98,14 @@ def test_config_refusals(lib, field, value, status):
     assert N.lib().moe_workspace_size(C.byref(cfg)) == 0
 
 
+def test_top_k_beyond_one_union_block_refused(lib):
+    """A row's top_k ids must fit one 64-id union block."""
+    cfg = good_cfg(num_experts=128, router_width=128, top_k=65)
+    with pytest.raises(N.MoeError):
+        N.moe_check_config(cfg)
+    N.moe_check_config(good_cfg(num_experts=128, router_width=128, top_k=64))
+
+
 def test_zero_computation_router_refused_as_unsupported(lib):
     cfg = good_cfg(router_width=20)
     with pytest.raises(N.MoeError) as ei:
@@ -133,8 +141,8 @@ def fake_weights():
 # case -> (expected status, text the error message must contain)
 FORWARD_REFUSALS = {
     "rows0": (1, "rows=0"),
-    "rows9": (1, "rows=9"),
-    "ids65": (2, "rows*top_k=80 exceeds 64"),
+    "rows33": (1, "rows=33"),
+    "ids257": (2, "rows*top_k=272 exceeds 256"),
     "x_null": (1, "x: NULL"),
     "x_misaligned": (1, "x: NULL or not 16-byte aligned"),
     "out_null": (1, "out is NULL"),
@@ -163,11 +171,11 @@ def test_forward_refusals_on_host(lib, case):
     x, out, rows, ws, nbytes = 0x200000, 0x400000, 2, 0x800000, need
     if case == "rows0":
         rows = 0
-    elif case == "rows9":
-        rows = 9
-    elif case == "ids65":
+    elif case == "rows33":
+        rows = 33
+    elif case == "ids257":
         cfg = good_cfg(top_k=16, num_experts=16, router_width=16)
-        rows = 5
+        rows = 17
     elif case == "x_null":
         x = 0
     elif case == "x_misaligned":
@@ -208,7 +216,7 @@ def test_forward_refusals_on_host(lib, case):
     assert text in N.lib().moe_last_error().decode()
 
 
-@pytest.mark.parametrize("case", ["rows0", "rows9", "x_null", "out_null", "overlap",
+@pytest.mark.parametrize("case", ["rows0", "rows33", "x_null", "out_null", "overlap",
                                   "table_null", "shared_misaligned"])
 def test_static_forward_refuses_before_any_device_call(lib, case):
     """moe_forward_static checks every argument before it looks up or clears
@@ -220,8 +228,8 @@ def test_static_forward_refuses_before_any_device_call(lib, case):
     x, out, rows = 0x200000, 0x400000, 2
     if case == "rows0":
         rows = 0
-    elif case == "rows9":
-        rows = 9
+    elif case == "rows33":
+        rows = 33
     elif case == "x_null":
         x = 0
     elif case == "out_null":

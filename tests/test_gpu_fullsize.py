@@ -32,6 +32,7 @@ CASES = [
     ("verify_h4096_e256", 2, 4, "wl"),
     ("prefill8_h2048_e512", 0, 8, "wl"),
     ("prefill8_h2048_e512", 1, 8, "corr"),
+    ("prefill8_h2048_e512", 2, 16, "wl"),     # two 8-row sub-chunks in one call
     ("sweep_h4096_e160", 0, 1, "wl"),
     ("sweep_h4096_e160", 5, 5, "wl"),
     ("sweep_h4096_e160", 47, 8, "wl"),

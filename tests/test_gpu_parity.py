@@ -159,11 +159,13 @@ def test_route_stage_logits_ids_weights():
 
 @pytest.mark.parametrize("per_row", [False, True])
 def test_union_stage_vs_oracle(per_row):
+    """moe_union on up to 32 rows (256 ids, four blocks of 64): the union
+    sequence, row masks and slot map bit-exact against the oracle's."""
     rng = np.random.default_rng(7)
     shape = S(num_experts=40, top_k=8)
     cfg = L.make_config(shape, per_row_mode=per_row)
     ws = L.Workspace(shape)
-    for rows in range(1, 9):
+    for rows in list(range(1, 9)) + [9, 12, 16, 23, 32]:
         for _ in range(5):
             pool = rng.choice(40, size=12, replace=False)   # overlapping rows
             ids = np.stack([rng.choice(pool, 8, replace=False) for _ in range(rows)])
@@ -307,3 +309,35 @@ def test_gemv_lever_ignored_above_one_row():
     a = G.gpu_run(weights, x)
     b = G.gpu_run(weights, x, gemv=True)
     assert torch.equal(a["out"].view(torch.int16), b["out"].view(torch.int16))
+
+
+PREFILL_SHAPES = {
+    "k8": S(num_experts=40, top_k=8),
+    "k4_sigmoid": S(num_experts=64, top_k=4, moe_inter=256, shared_inter=256,
+                    scoring="sigmoid", routed_scaling_factor=2.5),
+    "k3": S(num_experts=24, top_k=3, moe_inter=384, shared_inter=128),
+}
+
+
+@pytest.mark.parametrize("name", list(PREFILL_SHAPES))
+@pytest.mark.parametrize("rows", [9, 16, 32])
+def test_prefill_chunks_beyond_eight_rows(name, rows):
+    """Calls of more than one 8-row sub-chunk: oracle parity on every row, the
+    call's union (all rows, first-occurrence order across the sub-chunks)
+    bit-exact against the oracle's, union mode byte-identical to per-row
+    mode, and every row's bytes those of a call holding only its sub-chunk."""
+    shape = PREFILL_SHAPES[name]
+    rows = min(rows, 256 // shape.top_k)
+    corr = 0.7 if shape.scoring == "sigmoid" else 0.4
+    weights, x = G.make_case(shape, rows, seed_w=71, seed_x=72, corr=corr)
+    dl = L.DeviceLayer(weights)
+    res = G.gpu_run(weights, x, dl=dl)
+    G.check_parity(weights, x, res)
+    assert res["uni"]["rows"] == rows
+    pr = G.gpu_run(weights, x, per_row=True, dl=dl)
+    assert torch.equal(res["out"].view(torch.int16), pr["out"].view(torch.int16))
+    cr = min(8, 64 // shape.top_k)
+    for r0 in range(0, rows, cr):
+        sub_out = G.gpu_run(weights, x[r0:r0 + cr].contiguous(), dl=dl)["out"]
+        assert torch.equal(sub_out.view(torch.int16),
+                           res["out"][r0:r0 + cr].view(torch.int16))
