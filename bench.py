@@ -213,14 +213,14 @@ class ClockSampler:
 # Workload
 # ---------------------------------------------------------------------------
 
-def build_workload(name, rows, n_layers, device):
+def build_workload(name, rows, n_layers, device, t_layout=False):
     import torch
     from routed_moe_decode_router_gb300 import layer as L
     from routed_moe_decode_router_gb300 import synth
     wl = synth.WORKLOADS[name]
     shape = wl.shape
     layers = [L.DeviceLayer(synth.make_layer(shape, wl.seed_base + l, device=device),
-                            device=device) for l in range(n_layers)]
+                            device=device, t_layout=t_layout) for l in range(n_layers)]
     xbuf = torch.empty((n_layers, rows, shape.hidden), dtype=torch.bfloat16, device=device)
     for l in range(n_layers):
         xbuf[l] = synth.make_rows(shape, rows, seed=wl.seed_base + 500 + l, device=device,
@@ -435,9 +435,10 @@ def run_ours(args, rank, world, local):
     wl0 = synth.WORKLOADS[args.workload]
     rows = args.rows or max(wl0.rows)
     n_layers = args.layers or wl0.layers
-    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev)
+    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev,
+                                                     args.t_layout)
     from routed_moe_decode_router_gb300 import layer as L
-    ws = L.Workspace(shape, device=dev)
+    ws = L.Workspace(shape, device=dev, t_layout=args.t_layout)
     stream = torch.cuda.Stream(device=dev)
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
@@ -487,6 +488,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, bf16 activations)",
         "config": workload_config(wl, shape, rows, n_layers, {
             "gemv_lever": int(args.gemv and rows == 1),
+            "down_layout": "t (input-major)" if args.t_layout else "output-major",
             "union_mean": round(sum(U) / len(U), 3),
             "l2": "no flush: each step streams %.2f GB of distinct weights (L2 129 MB)"
                   % (step_bytes / 1e9),
@@ -598,6 +600,8 @@ def main(argv=None):
     ap.add_argument("--cpu-1core-s", type=float, default=5.0)
     ap.add_argument("--gemv", action="store_true",
                     help="one-row layers on the CUDA-core GEMV variant (gemv_lever = 1)")
+    ap.add_argument("--t-layout", action="store_true",
+                    help="down projections in the t layout (the fused one-row form)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the extra rows=1..8 workloads beside the headline line")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)

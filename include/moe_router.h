@@ -41,6 +41,18 @@
  *   scale2  fp32, one per matrix.
  *   weight[n][k] = e2m1(code) * e4m3(scale) * scale2.
  *   Both arrays must start on a 16-byte boundary.
+ *
+ * The same matrix in the t layout (the transposed decode layout that the
+ * forward_token_major.rs page names -- use_t_layout_for_decode -- without
+ * defining it; this library stores the down projections that way when
+ * moe_config.t_layout = 1): the same codes and the same 16-input scale
+ * blocks, stored input-major:
+ *   packed  uint8 [K][N/2]; element (n, k) in byte k * N/2 + n/2, the low
+ *           nibble holding the even output index;
+ *   scales  uint8 [K/16][N]; the scale of (n, inputs 16b .. 16b+15) in
+ *           byte b * N + n;
+ *   scale2  unchanged.
+ * moe_nvfp4_to_t_layout converts a matrix (or a stack of them).
  */
 #ifndef MOE_ROUTER_H
 #define MOE_ROUTER_H
@@ -58,7 +70,7 @@ extern "C" {
 #define MOE_API
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 #define MOE_MAX_ROWS 32       /* rows per call */
 #define MOE_MAX_IDS 256       /* rows * top_k per call (the union's capacity) */
 #define MOE_CHUNK_ROWS 8      /* rows per sub-chunk of the expert sweep ... */
@@ -122,7 +134,9 @@ typedef struct moe_config {
                                     pair streams its expert separately (the
                                     token-major reference order); the output
                                     is byte-identical to the union mode */
-    int gemv_lever;              /* one-row calls only (rows = 1): 0 = the
+    int gemv_lever;              /* one-row sub-chunks only (a one-row call,
+                                    or the one-row last sub-chunk of a
+                                    longer call; see moe_forward): 0 = the
                                     expert projections on the tensor cores
                                     (NVFP4 unpacked to f16, mma.sync, fp32
                                     accumulation); 1 = on the CUDA cores as
@@ -134,8 +148,17 @@ typedef struct moe_config {
                                     per-row mode are byte-identical within
                                     either.  The forward_ep.rs page switches
                                     its one-row GEMV kernels the same way
-                                    (ctx.levers.gemv_sw).  Rows > 1 ignore
-                                    it. */
+                                    (ctx.levers.gemv_sw).  Sub-chunks of
+                                    more rows ignore it. */
+    int t_layout;                /* 0: every down projection (routed and
+                                    shared) in the NVFP4 layout above,
+                                    [H][I/2] + [H][I/16]; 1: in the t layout
+                                    ([I][H/2] + [I/16][H]).  The t layout is
+                                    a decode layout: moe_forward then takes
+                                    every row as a sub-chunk of its own and
+                                    runs the fused one-row form (see
+                                    moe_forward).  Gate and up projections
+                                    keep the layout above either way. */
 } moe_config;
 
 /* Per-expert NVFP4 matrices: device arrays indexed by expert id
@@ -173,6 +196,18 @@ typedef struct moe_union_table {
     uint8_t uslot[MOE_MAX_IDS][MOE_MAX_ROWS]; /* [u][r]: slot of union[u] in
                                            row r, 0xFF if r did not pick it */
 } moe_union_table;
+
+/* Convert `count` NVFP4 matrices of N outputs x K inputs, stored back to
+ * back in the layout above (packed: count x [N][K/2], scales: count x
+ * [N][K/16]), into the t layout (packed_t: count x [K][N/2], scales_t: count
+ * x [K/16][N]), asynchronously on `stream`.  N and K: multiples of 16, 16 ..
+ * 65536; all four arrays device memory, 16-byte aligned, the outputs not
+ * overlapping the inputs.  A one-off load-time step (one launch), not part
+ * of the forward; scale2 is unchanged. */
+MOE_API moe_status moe_nvfp4_to_t_layout(const uint8_t *packed, const uint8_t *scales,
+                                         int count, int n_out, int k_in,
+                                         uint8_t *packed_t, uint8_t *scales_t,
+                                         void *stream);
 
 /* ABI version of the loaded library (MOE_ABI_VERSION when built). */
 MOE_API int moe_abi_version(void);
@@ -241,7 +276,16 @@ MOE_API moe_status moe_union(const moe_config *cfg, const moe_weights *w,
  * ids, one block) is swept once for all its rows, and every row's output
  * bytes are those a call with that sub-chunk alone would give.  A call of
  * more than one sub-chunk then resolves the union of all its rows (as
- * moe_union does) for moe_read_routing. */
+ * moe_union does) for moe_read_routing.
+ *
+ * With t_layout = 1 every row is a sub-chunk of its own and runs in a fused
+ * form: each 16-row gate/up tile's h goes straight into the 16 rows of the
+ * transposed down projection that it multiplies, every SM keeps a partial
+ * sum of every output, and after one grid barrier the partials are added in
+ * a fixed order (the down sweep, the blend and their two grid barriers do
+ * not exist in this form).  Its results agree with t_layout = 0 within the
+ * parity tolerance, not byte for byte; union and per-row mode give the same
+ * bytes. */
 MOE_API moe_status moe_forward(const moe_config *cfg, const moe_weights *w,
                        const uint16_t *x, uint16_t *out, int rows, void *ws,
                        size_t ws_bytes, void *stream);
@@ -258,8 +302,9 @@ MOE_API moe_status moe_forward_timed(const moe_config *cfg, const moe_weights *w
 
 /* Bytes of the library-owned device workspace behind moe_forward_static;
  * it covers every configuration moe_check_config accepts (at most about
- * 5.3 MB at hidden 4096, 1024 experts, intermediate 4096). */
-#define MOE_STATIC_WORKSPACE_BYTES (6u << 20)
+ * 9.3 MB, with the t layout at hidden 4096, 1024 experts, intermediate
+ * 4096). */
+#define MOE_STATIC_WORKSPACE_BYTES (10u << 20)
 
 /* moe_forward for callers that cannot allocate device memory themselves --
  * for example a plug-in running inside a host framework that owns every

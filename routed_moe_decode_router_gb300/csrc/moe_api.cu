@@ -16,7 +16,9 @@ namespace moe {
 cudaError_t launch_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_union(const UnionParams &p, cudaStream_t stream);
 cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
-                         bool gemv, cudaStream_t stream);
+                         bool gemv, bool t_layout, cudaStream_t stream);
+cudaError_t launch_t_layout(const uint8_t *packed, const uint8_t *scales, int count, int n_out,
+                            int k_in, uint8_t *packed_t, uint8_t *scales_t, cudaStream_t stream);
 cudaError_t set_layer_smem_limit(int bytes);
 size_t layer_smem_bytes(int stages, uint32_t slot_bytes);
 }  // namespace moe
@@ -111,9 +113,9 @@ moe_status check_cfg(const moe_config *c) {
     if (c->router_fmt != MOE_ROUTER_BF16 && c->router_fmt != MOE_ROUTER_NVFP4)
         return fail(MOE_ERR_INVALID_ARG, "router_fmt=%d: must be bf16 (0) or nvfp4 (1)",
                     c->router_fmt);
-    if ((c->norm_topk_prob | c->shared_gate | c->per_row_mode | c->gemv_lever) & ~1)
+    if ((c->norm_topk_prob | c->shared_gate | c->per_row_mode | c->gemv_lever | c->t_layout) & ~1)
         return fail(MOE_ERR_INVALID_ARG,
-                    "norm_topk_prob, shared_gate, per_row_mode, gemv_lever are 0/1");
+                    "norm_topk_prob, shared_gate, per_row_mode, gemv_lever, t_layout are 0/1");
     return MOE_OK;
 }
 
@@ -395,14 +397,21 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     // Ring slot = one 16-row gate or up tile (16 x H/2 packed + 16 x H/16
     // scale bytes) or one down tile (down_rows x I/2 + down_rows x I/16); a
     // gate+up unit takes two slots, a down unit one.
+    // In the t layout a unit's third slot holds its 16 rows of the
+    // transposed down matrix (16 x H/2 + H bytes: the size of a gate tile),
+    // and there are no down units.
+    const bool tl = cfg->t_layout != 0;
     const size_t gu_slot = (size_t)kTileRows * (cfg->hidden / 2 + cfg->hidden / 16);
-    const size_t d_slot = (size_t)lp.down_rows * (L.inter_max / 2 + L.inter_max / 16);
+    const size_t d_slot = tl ? 0 : (size_t)lp.down_rows * (L.inter_max / 2 + L.inter_max / 16);
     lp.slot_bytes = (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot);
     const int budget = di->smem_optin - 1024;
     int S = 16;
     while (S > 2 && layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget) --S;
-    if (layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget)
+    if (layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget || (tl && S < 4))
         return fail(MOE_ERR_UNSUPPORTED, "stage ring does not fit in shared memory");
+    if (tl && di->sms > kMaxTCtas)
+        return fail(MOE_ERR_UNSUPPORTED, "t layout: %d SMs, the workspace holds partials of %d",
+                    di->sms, kMaxTCtas);
     lp.stages = S;
     const int mc_gu = (cfg->hidden / kChunk + kConsumerWarps - 1) / kConsumerWarps;
     const int mc_d = lp.down_split ? L.inter_max / kChunk / 4
@@ -410,7 +419,7 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
 
     // one launch per sub-chunk of at most 8 rows (64 ids), in row order; a
     // call of several sub-chunks then resolves the union of all its rows
-    const int cr = chunk_rows(cfg), H = cfg->hidden;
+    const int cr = tl ? 1 : chunk_rows(cfg), H = cfg->hidden;
     const int nchunks = (rows + cr - 1) / cr;
     cudaError_t e = cudaSuccess;
     if (ev) e = cudaEventRecord(static_cast<cudaEvent_t>(ev[0]), st);
@@ -421,8 +430,10 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
         lp.publish_union = nchunks == 1;
         lp.x = x + (size_t)r0 * H;
         lp.out = out + (size_t)r0 * H;
-        e = launch_layer(lp, di->sms, layer_smem_bytes(S, lp.slot_bytes), mc_gu, mc_d,
-                         rows == 1 && cfg->gemv_lever, st);
+        // gemv_lever applies per sub-chunk, so that a one-row last sub-chunk
+        // gives the bytes of a one-row call
+        e = launch_layer(lp, di->sms, layer_smem_bytes(S, lp.slot_bytes), mc_gu, tl ? 1 : mc_d,
+                         n == 1 && cfg->gemv_lever, tl, st);
     }
     if (e == cudaSuccess && nchunks > 1)
         e = launch_union(union_params(cfg, w, lp.ws.ids, rows, lp.ws, nullptr), st);
@@ -436,6 +447,33 @@ extern "C" {
 moe_status moe_forward(const moe_config *cfg, const moe_weights *w, const uint16_t *x,
                        uint16_t *out, int rows, void *ws, size_t ws_bytes, void *stream) {
     return forward_impl(cfg, w, x, out, rows, ws, ws_bytes, stream, nullptr);
+}
+
+moe_status moe_nvfp4_to_t_layout(const uint8_t *packed, const uint8_t *scales, int count,
+                                 int n_out, int k_in, uint8_t *packed_t, uint8_t *scales_t,
+                                 void *stream) {
+    if (count < 1) return fail(MOE_ERR_INVALID_ARG, "count=%d: must be at least 1", count);
+    if (n_out < 16 || n_out > 65536 || n_out % 16 || k_in < 16 || k_in > 65536 || k_in % 16)
+        return fail(MOE_ERR_INVALID_ARG,
+                    "n_out=%d, k_in=%d: each must be a multiple of 16 in [16, 65536]", n_out, k_in);
+    if (!packed || !scales || !packed_t || !scales_t)
+        return fail(MOE_ERR_INVALID_ARG, "a matrix pointer is NULL");
+    if (!aligned(packed, 16) || !aligned(scales, 16) || !aligned(packed_t, 16) ||
+        !aligned(scales_t, 16))
+        return fail(MOE_ERR_INVALID_ARG, "matrix pointers must be 16-byte aligned");
+    const size_t pk = (size_t)count * n_out * (k_in / 2), sc = (size_t)count * n_out * (k_in / 16);
+    auto overlap = [](const void *a, size_t na, const void *b, size_t nb) {
+        const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+        return x < y + nb && y < x + na;
+    };
+    if (overlap(packed_t, pk, packed, pk) || overlap(packed_t, pk, scales, sc) ||
+        overlap(scales_t, sc, packed, pk) || overlap(scales_t, sc, scales, sc) ||
+        overlap(packed_t, pk, scales_t, sc))
+        return fail(MOE_ERR_INVALID_ARG, "the t-layout outputs overlap each other or the inputs");
+    const cudaError_t e = launch_t_layout(packed, scales, count, n_out, k_in, packed_t, scales_t,
+                                          static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "t-layout launch: %s", cudaGetErrorString(e));
+    return ok();
 }
 
 moe_status moe_forward_timed(const moe_config *cfg, const moe_weights *w, const uint16_t *x,

@@ -2,8 +2,9 @@
 // kernel selection (MC_GU, MC_D, top-k class, projection variant) and the
 // cooperative, PDL launch.  The kernel itself is in moe_layer_kernel.cuh,
 // instantiated in moe_layer_tk0.cu .. moe_layer_tk3.cu (tensor-core
-// projections) and moe_layer_tk0_gv.cu .. moe_layer_tk3_gv.cu (the one-row
-// CUDA-core GEMV).
+// projections), moe_layer_tk0_gv.cu .. moe_layer_tk3_gv.cu (the one-row
+// CUDA-core GEMV) and moe_layer_tk0_t.cu .. moe_layer_tk3_t.cu (the fused
+// one-row form for down projections in the t layout, both variants).
 #include <cuda_runtime.h>
 
 #include "moe_layout.h"
@@ -18,6 +19,10 @@ void *layer_kernel_tk0_gv(int mc_gu, int mc_d);
 void *layer_kernel_tk1_gv(int mc_gu, int mc_d);
 void *layer_kernel_tk2_gv(int mc_gu, int mc_d);
 void *layer_kernel_tk3_gv(int mc_gu, int mc_d);
+void *layer_kernel_tk0_t(int mc_gu, bool gv);
+void *layer_kernel_tk1_t(int mc_gu, bool gv);
+void *layer_kernel_tk2_t(int mc_gu, bool gv);
+void *layer_kernel_tk3_t(int mc_gu, bool gv);
 size_t layer_fixed_smem_bytes();
 
 size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
@@ -28,7 +33,15 @@ size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
 // in registers: 4, 8, 16 or two lists of 16).
 static int topk_class(int E) { return E <= 128 ? 0 : (E <= 256 ? 1 : (E <= 512 ? 2 : 3)); }
 
-static void *layer_kernel(int mc_gu, int mc_d, int tk, bool gv) {
+static void *layer_kernel(int mc_gu, int mc_d, int tk, bool gv, bool tl) {
+    if (tl) {
+        switch (tk) {
+        case 0: return layer_kernel_tk0_t(mc_gu, gv);
+        case 1: return layer_kernel_tk1_t(mc_gu, gv);
+        case 2: return layer_kernel_tk2_t(mc_gu, gv);
+        default: return layer_kernel_tk3_t(mc_gu, gv);
+        }
+    }
     switch (tk) {
     case 0: return gv ? layer_kernel_tk0_gv(mc_gu, mc_d) : layer_kernel_tk0(mc_gu, mc_d);
     case 1: return gv ? layer_kernel_tk1_gv(mc_gu, mc_d) : layer_kernel_tk1(mc_gu, mc_d);
@@ -41,18 +54,20 @@ cudaError_t set_layer_smem_limit(int bytes) {
     for (int v = 0; v < 2; ++v)
         for (int t = 0; t < 4; ++t)
             for (int a = 1; a <= 4; ++a)
-                for (int b = 1; b <= 4; ++b) {
-                    cudaError_t e = cudaFuncSetAttribute(layer_kernel(a, b, t, v != 0),
-                                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                         bytes);
-                    if (e != cudaSuccess) return e;
-                }
+                for (int b = 1; b <= 4; ++b)
+                    // (MC_D = 1 also stands for the t-layout form of this MC_GU)
+                    for (int tl = 0; tl < (b == 1 ? 2 : 1); ++tl) {
+                        cudaError_t e = cudaFuncSetAttribute(
+                            layer_kernel(a, b, t, v != 0, tl != 0),
+                            cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+                        if (e != cudaSuccess) return e;
+                    }
     return cudaSuccess;
 }
 
 cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
-                         bool gemv, cudaStream_t stream) {
-    void *fn = layer_kernel(mc_gu, mc_d, topk_class(p.E), gemv);
+                         bool gemv, bool t_layout, cudaStream_t stream) {
+    void *fn = layer_kernel(mc_gu, mc_d, topk_class(p.E), gemv, t_layout);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -38,9 +38,17 @@
 // unit one.  The MMA is mma.sync m16n8k16 (f16 x f16 -> fp32) with the NVFP4
 // weights unpacked to f16 in registers and the token rows as the 8 columns.
 //
-// Every wait is bounded (ring waits, the three grid barriers); a wait that
-// runs out records MOE_DEV_WAIT_TIMEOUT, and the CTA skips the rest of its
-// work.
+// With the down projections in the t layout (input-major, one row per
+// intermediate index; one token row per launch) the layer is fused instead:
+// each gate+up unit also streams its 16 rows of the transposed down matrix
+// (a third ring slot), the compute warps apply them to the unit's h as soon
+// as the epilogue warp has formed it, and each CTA keeps a partial sum of
+// every output; after phase C one grid barrier, then CTA b adds up its slice
+// of the outputs over all CTAs' partials in CTA order.  Phases D and E and
+// grid barrier 3 do not exist in this form.
+//
+// Every wait is bounded (ring waits, the grid barriers); a wait that runs
+// out records MOE_DEV_WAIT_TIMEOUT, and the CTA skips the rest of its work.
 #pragma once
 #include <cuda_runtime.h>
 
@@ -97,6 +105,11 @@ struct LayerSmem {
     uint32_t umask[kMaxIds];
     uint64_t red_full[kRed];                    // partials ready (8 compute-warp arrivals)
     uint64_t red_empty[kRed];                   // partials consumed (1 epilogue arrival)
+    // t layout: the h values of a gate+up unit, handed from the epilogue
+    // warp that formed them to the compute warps (one slot per epilogue warp)
+    float hsm[kEpiWarps][kTileRows];
+    uint64_t h_full[kEpiWarps];                 // h written (1 epilogue arrival)
+    uint64_t h_empty[kEpiWarps];                // h read (8 compute-warp arrivals)
     unsigned long long *bar;                    // this launch's grid-barrier counter
     int abort;
 };
@@ -143,8 +156,9 @@ __device__ __forceinline__ void router_decode(const LayerParams &p, int row, uin
 // phases; TK: the top-k class of the router width (0: E <= 128, 1: <= 256,
 // 2: <= 512, 3: <= 1024), so each instantiation holds one top-k variant;
 // GV: the one-row CUDA-core GEMV variant of the expert projections
-// (chunk_gemv) instead of the tensor-core MMA (chunk_mma).
-template <int MC_GU, int MC_D, int TK, bool GV>
+// (chunk_gemv) instead of the tensor-core MMA (chunk_mma); TL: the fused
+// one-row form for down projections in the t layout (MC_D unused).
+template <int MC_GU, int MC_D, int TK, bool GV, bool TL>
 __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const LayerParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     LayerSmem &sm = *reinterpret_cast<LayerSmem *>(smem);
@@ -187,6 +201,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             mbar_init(&sm.red_full[r], kConsumerWarps);
             mbar_init(&sm.red_empty[r], 1);
         }
+        for (int r = 0; r < kEpiWarps; ++r) {
+            mbar_init(&sm.h_full[r], 1);
+            mbar_init(&sm.h_empty[r], kConsumerWarps);
+        }
         fence_mbar_init();
         sm.abort = 0;
     }
@@ -214,34 +232,51 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         ++pi;
         return true;
     };
-    // gate+up unit j (16 rows): a gate slot, then an up slot
+    // gate+up unit j (16 rows): a gate slot, then an up slot; in the t
+    // layout also a slot with the unit's 16 rows of the transposed down
+    // matrix (16 x H/2 packed bytes, then the H scales of that block)
+    constexpr int kUnitSlots = TL ? 3 : 2;
+    const uint32_t dt_pk = kTileRows * H / 2, dt_sc = H;
     auto issue_gu = [&](int j) -> bool {
-        const uint8_t *gp, *gs, *upk, *us;
+        const uint8_t *gp, *gs, *upk, *us, *dp = nullptr, *ds = nullptr;
         if (j < St) {
             gp = p.sh_gate.packed + (size_t)j * gu_pk;
             gs = p.sh_gate.scales + (size_t)j * gu_sc;
             upk = p.sh_up.packed + (size_t)j * gu_pk;
             us = p.sh_up.scales + (size_t)j * gu_sc;
+            if (TL) {
+                dp = p.sh_down.packed + (size_t)j * dt_pk;
+                ds = p.sh_down.scales + (size_t)j * dt_sc;
+            }
         } else {
             const PtrEntry &e = sm.ptrs[(j - St) / It];
             const int tile = (j - St) % It;
-            if (e.expert < 0) return issue_empty() && issue_empty();
+            if (e.expert < 0)
+                return issue_empty() && issue_empty() && (!TL || issue_empty());
             gp = e.packed[0] + (size_t)tile * gu_pk;
             gs = e.scales[0] + (size_t)tile * gu_sc;
             upk = e.packed[1] + (size_t)tile * gu_pk;
             us = e.scales[1] + (size_t)tile * gu_sc;
+            if (TL) {
+                dp = e.packed[2] + (size_t)tile * dt_pk;
+                ds = e.scales[2] + (size_t)tile * dt_sc;
+            }
         }
         if (!acquire(pi)) return false;
         issue_pair(gp, gs, gu_pk, gu_sc);
         if (!acquire(pi)) return false;
         issue_pair(upk, us, gu_pk, gu_sc);
+        if (TL) {
+            if (!acquire(pi)) return false;
+            issue_pair(dp, ds, dt_pk, dt_sc);
+        }
         return true;
     };
 
     int pj = b;   // next gate+up unit of this CTA
     if (is_prod && lane == 0) {
         pol = l2_evict_first_policy();
-        while (pj < St && pi + 2 <= S) {
+        while (pj < St && pi + kUnitSlots <= S) {
             issue_gu(pj);
             pj += G;
         }
@@ -437,7 +472,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         if (lane == 0) {
             bool ok = true;
             for (; ok && pj < Tgu; pj += G) ok = issue_gu(pj);
-            for (int j = d_begin; ok && j < d_end; ++j) {
+            for (int j = d_begin; !TL && ok && j < d_end; ++j) {
                 const uint8_t *dp, *ds;
                 int K;
                 if (j < Sd) {
@@ -518,7 +553,26 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 us[0] += on ? ua[w].x : 0.f; us[1] += on ? ua[w].y : 0.f;
                 us[2] += on ? ua[w].z : 0.f; us[3] += on ? ua[w].w : 0.f;
             }
-            if (live && !*abort) {
+            if constexpr (TL) {
+                // the unit's 16 h values (token row 0: lanes 0..3, rounded
+                // to bf16) to this warp's slot, once the compute warps have
+                // read its previous use
+                float hf[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    hf[i] = bf16_lo(f2bf16_rn(silu(gs[i] * s2g) * (us[i] * s2u)));
+                const int hb = epi_idx;
+                if (ui >= kEpiWarps)
+                    ring_wait(&sm.h_empty[hb], ((ui / kEpiWarps) - 1) & 1, abort, hdr,
+                              0x500000u + (uint32_t)ui);
+                if (col == 0) {
+                    const bool on = live && !*abort;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sm.hsm[hb][4 * rq + i] = on ? hf[i] : 0.f;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.h_full[hb]);
+            } else if (live && !*abort) {
                 uint32_t hv[2];
 #pragma unroll
                 for (int i = 0; i < 2; ++i) {
@@ -535,6 +589,16 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                                            tile * kTileRows + 4 * rq) = make_uint2(hv[0], hv[1]);
             }
             MOE_TOC(lane == 0, 26, t_ex);
+        }
+        if constexpr (TL) {
+            // the compute warps finish the layer (partial outputs, grid
+            // barrier, sum over the CTAs); the epilogue warps take the grid
+            // barrier for them
+            named_bar(3, kComputeAndEpi);   // every partial of this CTA stored
+            MOE_PHASE_MARK(lane == 0 && epi_idx == 0, 13);
+            if (lane == 0 && epi_idx == 0) grid_arrive_wait(sm.bar, G, abort, hdr, 2u);
+            named_bar(3, kComputeAndEpi);   // every CTA's partials visible
+            return;
         }
         // every h of this CTA is stored (both epilogue warps): grid barrier,
         // then release the compute warps
@@ -701,6 +765,91 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             return rb;
         };
 
+        // t layout: compute thread tid owns outputs 8 tid + 2048 g .. + 7
+        // (g < NG) and keeps this CTA's partial sums of them.  A unit's down
+        // block (its third slot) is applied after the next unit's MMAs, once
+        // the epilogue warp has handed over the unit's h: each output's 16
+        // products are summed in f16 in two halves of 8 (h scaled so that
+        // its largest magnitude lies in [2^8, 2^9): no partial can exceed
+        // 8 * 6 * 2^9 < 65504), the halves and the block scale in fp32.
+        constexpr int NG = TL ? (MC_GU + 1) / 2 : 1;
+        float yacc[NG][8];
+#pragma unroll
+        for (int gi = 0; gi < NG; ++gi)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) yacc[gi][i] = 0.f;
+        auto tl_apply = [&](int j, int uij, int s, uint32_t par) {
+            const int hb = uij % kEpiWarps;
+            ring_wait(&sm.h_full[hb], (uij / kEpiWarps) & 1, abort, hdr, 0x600000u + (uint32_t)uij);
+            float hv[kTileRows];
+#pragma unroll
+            for (int i = 0; i < kTileRows; ++i) hv[i] = sm.hsm[hb][i];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.h_empty[hb]);
+            const bool okd = ring_wait(&full[s], par, abort, hdr, 0x700000u + (uint32_t)uij);
+            bool live = true;
+            float coef;
+            if (j < St) {
+                coef = sm.gate_val[0] * p.sh_down.scale2;
+            } else {
+                const int e = (j - St) / It;
+                live = sm.ptrs[e].expert >= 0;
+                coef = live ? sm.wts[sm.uni.uslot[e][0]] * sm.ptrs[e].scale2[2] : 0.f;
+            }
+            if (okd && live) {
+                float mx = 0.f;
+#pragma unroll
+                for (int i = 0; i < kTileRows; ++i) mx = fmaxf(mx, fabsf(hv[i]));
+                const int ex = max(f16_block_exponent(mx) - 6, -126);
+                const float up = exp2i(ex);
+                coef *= exp2i(-ex);
+                uint32_t h2[kTileRows];
+#pragma unroll
+                for (int i = 0; i < kTileRows; ++i) h2[i] = pack_f16x2(hv[i] * up, hv[i] * up);
+                const uint8_t *blk = ring + (size_t)s * p.slot_bytes;
+#pragma unroll
+                for (int gi = 0; gi < NG; ++gi) {
+                    const int o0 = 8 * tid + 2048 * gi;
+                    if (o0 < H) {
+                        __half2 acc[2][4];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) acc[hh][i] = __float2half2_rn(0.f);
+#pragma unroll
+                        for (int kk = 0; kk < kTileRows; ++kk) {
+                            const uint32_t w =
+                                *reinterpret_cast<const uint32_t *>(blk + kk * (H / 2) + o0 / 2);
+                            uint32_t qv[4];
+                            e2m1x8_to_f16x2(w, qv);
+                            const __half2 hk = *reinterpret_cast<const __half2 *>(&h2[kk]);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                acc[kk >> 3][i] = __hfma2(*reinterpret_cast<const __half2 *>(&qv[i]),
+                                                          hk, acc[kk >> 3][i]);
+                        }
+                        const uint2 sc8 = *reinterpret_cast<const uint2 *>(blk + dt_pk + o0);
+                        const uint32_t sw[4] = {e4m3x2_to_f16x2(sc8.x & 0xFFFFu),
+                                                e4m3x2_to_f16x2(sc8.x >> 16),
+                                                e4m3x2_to_f16x2(sc8.y & 0xFFFFu),
+                                                e4m3x2_to_f16x2(sc8.y >> 16)};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float2 sv = __half22float2(*reinterpret_cast<const __half2 *>(&sw[i]));
+                            const float2 lo = __half22float2(acc[0][i]);
+                            const float2 hi = __half22float2(acc[1][i]);
+                            yacc[gi][2 * i] = fmaf(coef * sv.x, lo.x + hi.x, yacc[gi][2 * i]);
+                            yacc[gi][2 * i + 1] = fmaf(coef * sv.y, lo.y + hi.y, yacc[gi][2 * i + 1]);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        };
+        int tl_j = -1, tl_ui = 0, tl_s = 0;   // the unit whose down block waits
+        uint32_t tl_p = 0u;
+
         // phase C: gate + up (both slots of a unit, the two matrices interleaved)
         {
             uint32_t bx[MC_GU][8][2];
@@ -718,6 +867,13 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 const int s1 = rs;
                 const uint32_t p1 = rp;
                 next_slot();
+                int s2 = 0;
+                uint32_t p2 = 0u;
+                if constexpr (TL) {
+                    s2 = rs;
+                    p2 = rp;
+                    next_slot();
+                }
                 MOE_TIC(t_w);
                 const bool ok0 = ring_wait(&full[s0], p0, abort, hdr, (uint32_t)ci);
                 const bool ok1 = ring_wait(&full[s1], p1, abort, hdr, (uint32_t)ci + 1);
@@ -766,9 +922,59 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sm.red_full[rb]);
                 ++ui;
+                if constexpr (TL) {
+                    if (tl_j >= 0) tl_apply(tl_j, tl_ui, tl_s, tl_p);
+                    tl_j = j;
+                    tl_ui = ui - 1;
+                    tl_s = s2;
+                    tl_p = p2;
+                }
             }
         }
         MOE_PHASE_MARK(tid == 0, 6);
+        if constexpr (TL) {
+            if (tl_j >= 0) tl_apply(tl_j, tl_ui, tl_s, tl_p);
+            // this CTA's partial outputs; after the grid barrier (taken by
+            // the epilogue warp) CTA b sums its slice of outputs over every
+            // CTA's partials: tpo threads per output, each adding the CTAs
+            // pg, pg + tpo, ... in order, then a fixed butterfly, so the
+            // bytes do not depend on timing
+            float *ypart = p.ws.ypart + (size_t)b * H;
+#pragma unroll
+            for (int gi = 0; gi < NG; ++gi) {
+                const int o0 = 8 * tid + 2048 * gi;
+                if (o0 < H) {
+                    *reinterpret_cast<float4 *>(ypart + o0) =
+                        make_float4(yacc[gi][0], yacc[gi][1], yacc[gi][2], yacc[gi][3]);
+                    *reinterpret_cast<float4 *>(ypart + o0 + 4) =
+                        make_float4(yacc[gi][4], yacc[gi][5], yacc[gi][6], yacc[gi][7]);
+                }
+            }
+            named_bar(3, kComputeAndEpi);   // every partial of this CTA stored
+            named_bar(3, kComputeAndEpi);   // the grid barrier passed
+            MOE_PHASE_MARK(tid == 0, 7);
+            const int per = (H + G - 1) / G;
+            int lg = 4;
+            while (lg > 0 && (per << lg) > kConsumerWarps * 32) --lg;
+            const int tpo = 1 << lg;
+            const int oi = tid >> lg, pg = tid & (tpo - 1);
+            const int o = b * per + oi;
+            const bool mine = oi < per && o < H;
+            const float *src = p.ws.ypart + (mine ? o : 0);
+            float s = 0.f;
+            for (int b0 = pg; b0 < G; b0 += 8 * tpo) {
+                float v[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = ld_cg(src + (size_t)min(b0 + tpo * i, G - 1) * H);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (b0 + tpo * i < G) s += v[i];
+            }
+            for (int off = tpo >> 1; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (mine && pg == 0 && !*abort) p.out[o] = f2bf16_rn(s);
+            MOE_PHASE_MARK(tid == 0, 9);
+            return;
+        }
         // wait until the epilogue warp has passed the grid barrier (every h written)
         named_bar(2, kComputeAndEpi);
         MOE_PHASE_MARK(tid == 0, 7);
@@ -937,16 +1143,29 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
 template <int TK, bool GV>
 void *layer_kernel_table(int mc_gu, int mc_d) {
     static void *const tab[4][4] = {
-        {(void *)moe_layer_kernel<1, 1, TK, GV>, (void *)moe_layer_kernel<1, 2, TK, GV>,
-         (void *)moe_layer_kernel<1, 3, TK, GV>, (void *)moe_layer_kernel<1, 4, TK, GV>},
-        {(void *)moe_layer_kernel<2, 1, TK, GV>, (void *)moe_layer_kernel<2, 2, TK, GV>,
-         (void *)moe_layer_kernel<2, 3, TK, GV>, (void *)moe_layer_kernel<2, 4, TK, GV>},
-        {(void *)moe_layer_kernel<3, 1, TK, GV>, (void *)moe_layer_kernel<3, 2, TK, GV>,
-         (void *)moe_layer_kernel<3, 3, TK, GV>, (void *)moe_layer_kernel<3, 4, TK, GV>},
-        {(void *)moe_layer_kernel<4, 1, TK, GV>, (void *)moe_layer_kernel<4, 2, TK, GV>,
-         (void *)moe_layer_kernel<4, 3, TK, GV>, (void *)moe_layer_kernel<4, 4, TK, GV>}};
+        {(void *)moe_layer_kernel<1, 1, TK, GV, false>, (void *)moe_layer_kernel<1, 2, TK, GV, false>,
+         (void *)moe_layer_kernel<1, 3, TK, GV, false>, (void *)moe_layer_kernel<1, 4, TK, GV, false>},
+        {(void *)moe_layer_kernel<2, 1, TK, GV, false>, (void *)moe_layer_kernel<2, 2, TK, GV, false>,
+         (void *)moe_layer_kernel<2, 3, TK, GV, false>, (void *)moe_layer_kernel<2, 4, TK, GV, false>},
+        {(void *)moe_layer_kernel<3, 1, TK, GV, false>, (void *)moe_layer_kernel<3, 2, TK, GV, false>,
+         (void *)moe_layer_kernel<3, 3, TK, GV, false>, (void *)moe_layer_kernel<3, 4, TK, GV, false>},
+        {(void *)moe_layer_kernel<4, 1, TK, GV, false>, (void *)moe_layer_kernel<4, 2, TK, GV, false>,
+         (void *)moe_layer_kernel<4, 3, TK, GV, false>, (void *)moe_layer_kernel<4, 4, TK, GV, false>}};
     if (mc_gu < 1 || mc_gu > 4 || mc_d < 1 || mc_d > 4) return nullptr;
     return tab[mc_gu - 1][mc_d - 1];
+}
+
+// The t-layout (fused one-row) instantiations of one top-k class: MC_GU
+// 1..4, both projection variants.
+template <int TK>
+void *layer_kernel_t_table(int mc_gu, bool gv) {
+    static void *const tab[2][4] = {
+        {(void *)moe_layer_kernel<1, 1, TK, false, true>, (void *)moe_layer_kernel<2, 1, TK, false, true>,
+         (void *)moe_layer_kernel<3, 1, TK, false, true>, (void *)moe_layer_kernel<4, 1, TK, false, true>},
+        {(void *)moe_layer_kernel<1, 1, TK, true, true>, (void *)moe_layer_kernel<2, 1, TK, true, true>,
+         (void *)moe_layer_kernel<3, 1, TK, true, true>, (void *)moe_layer_kernel<4, 1, TK, true, true>}};
+    if (mc_gu < 1 || mc_gu > 4) return nullptr;
+    return tab[gv ? 1 : 0][mc_gu - 1];
 }
 
 }  // namespace moe

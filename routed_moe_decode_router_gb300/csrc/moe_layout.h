@@ -37,6 +37,9 @@ constexpr int kConsumerWarps = 8;        // compute warps of the layer kernel
 constexpr int kRouteWarps = 8;
 // Layer kernel block: 8 compute warps, 2 epilogue warps, 1 producer warp.
 constexpr int kLayerBlockThreads = (kConsumerWarps + 3) * 32;
+// CTAs of a t-layout launch whose partial outputs the workspace holds (one
+// per SM of the device: at most 256).
+constexpr int kMaxTCtas = 256;
 
 // Status word and counters at the start of the workspace (256 bytes).
 //
@@ -76,7 +79,7 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // sub-chunk (8 rows), which the sub-chunks of a call reuse in turn.  One
 // workspace serves every row count.
 struct WsLayout {
-    size_t header, ids, wts, logits, gate_val, uni, ptrs, hbuf, ybuf, ysbuf, total;
+    size_t header, ids, wts, logits, gate_val, uni, ptrs, hbuf, ybuf, ysbuf, ypart, total;
     int inter_max;          // max(I, Is): row stride of the h buffer
 
     static WsLayout make(const moe_config &c) {
@@ -95,6 +98,8 @@ struct WsLayout {
         L.hbuf = o;     o = align256(o + 2 * (size_t)kEntries * kMaxRows * L.inter_max);
         L.ybuf = o;     o = align256(o + sizeof(float) * (size_t)kMaxIds * c.hidden);
         L.ysbuf = o;    o = align256(o + sizeof(float) * (size_t)kMaxRows * c.hidden);
+        // t layout: one partial output row per CTA
+        L.ypart = o;    o = align256(o + (c.t_layout ? sizeof(float) * (size_t)kMaxTCtas * c.hidden : 0));
         L.total = o;
         return L;
     }
@@ -112,6 +117,7 @@ struct WsPtrs {
     uint16_t *hbuf;   // bf16 [kEntries][kMaxRows][inter_max]
     float *ybuf;      // fp32 [kMaxIds][H]: position p = row * top_k + slot
     float *ysbuf;     // fp32 [kMaxRows][H]: shared expert output
+    float *ypart;     // fp32 [kMaxTCtas][H]: per-CTA partial outputs (t layout)
     int inter_max;
 };
 
@@ -128,6 +134,7 @@ inline WsPtrs ws_ptrs(void *ws, const WsLayout &L) {
     p.hbuf = reinterpret_cast<uint16_t *>(b + L.hbuf);
     p.ybuf = reinterpret_cast<float *>(b + L.ybuf);
     p.ysbuf = reinterpret_cast<float *>(b + L.ysbuf);
+    p.ypart = reinterpret_cast<float *>(b + L.ypart);
     p.inter_max = L.inter_max;
     return p;
 }

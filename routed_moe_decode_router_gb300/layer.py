@@ -11,10 +11,11 @@ from typing import Optional
 import torch
 
 from . import native as N
-from .synth import MoeLayerWeights, MoeShape
+from .synth import MoeLayerWeights, MoeShape, Nvfp4
 
 
-def make_config(shape: MoeShape, per_row_mode: bool = False, gemv: bool = False) -> N.MoeConfig:
+def make_config(shape: MoeShape, per_row_mode: bool = False, gemv: bool = False,
+                t_layout: bool = False) -> N.MoeConfig:
     return N.MoeConfig(
         hidden=shape.hidden, num_experts=shape.num_experts,
         router_width=shape.num_experts, top_k=shape.top_k,
@@ -24,7 +25,7 @@ def make_config(shape: MoeShape, per_row_mode: bool = False, gemv: bool = False)
         routed_scaling_factor=float(shape.routed_scaling_factor),
         router_fmt=N.MOE_ROUTER_NVFP4 if shape.router_fmt == "nvfp4" else N.MOE_ROUTER_BF16,
         has_shared=int(shape.has_shared), shared_gate=int(shape.shared_gated),
-        per_row_mode=int(per_row_mode), gemv_lever=int(gemv))
+        per_row_mode=int(per_row_mode), gemv_lever=int(gemv), t_layout=int(t_layout))
 
 
 def _ptr(t: Optional[torch.Tensor]) -> int:
@@ -70,17 +71,31 @@ class DeviceLayer:
 
     ``layer`` holds the weights (moved to ``device`` if needed).  The
     per-expert pointer tables (device arrays of pointers, indexed by expert
-    id) are built here once."""
+    id) are built here once.  With ``t_layout`` the down projections (routed
+    and shared) are converted once, by the library, into the t layout, and
+    the layer's calls run the fused one-row form; the layer then holds the
+    converted copies (the original down tensors stay in ``layer``)."""
 
-    def __init__(self, layer: MoeLayerWeights, device="cuda"):
+    def __init__(self, layer: MoeLayerWeights, device="cuda", t_layout: bool = False):
         if layer.device != torch.device(device) and str(layer.device) != str(device):
             layer = layer.to(device)
         self.layer = layer
         self.shape = layer.shape
         self.device = layer.gate.packed.device
+        self.t_layout = bool(t_layout)
         s = self.shape
         E = s.num_experts
         self._tables = {}
+        down = layer.down
+        sh_down = layer.sh_down if s.has_shared else None
+        if self.t_layout:
+            stream = _stream(None)
+            down = self._to_t(down, E, s.hidden, s.moe_inter, stream)
+            if s.has_shared:
+                sh_down = self._to_t(sh_down, 1, s.hidden, s.shared_inter, stream)
+        # the converted copies must live as long as the layer: the pointer
+        # tables and descriptors below point into them
+        self.down, self.sh_down = down, sh_down
         w = N.MoeWeights()
         if s.router_fmt == "nvfp4":
             m = layer.router_nvfp4
@@ -91,7 +106,7 @@ class DeviceLayer:
         if layer.bias is not None:
             w.correction_bias = layer.bias.data_ptr()
         for name in ("gate", "up", "down"):
-            m = getattr(layer, name)
+            m = down if name == "down" else getattr(layer, name)
             pk = m.packed.reshape(E, -1)
             sc = m.scales.reshape(E, -1)
             pk_ptrs = (pk.data_ptr() + torch.arange(E, dtype=torch.int64) *
@@ -106,13 +121,13 @@ class DeviceLayer:
             for name, field in (("sh_gate", "shared_gate_proj"),
                                 ("sh_up", "shared_up_proj"),
                                 ("sh_down", "shared_down_proj")):
-                m = getattr(layer, name)
+                m = sh_down if name == "sh_down" else getattr(layer, name)
                 setattr(w, field, N.Nvfp4Desc(m.packed.data_ptr(), m.scales.data_ptr(),
                                               float(m.scale2)))
             if s.shared_gated:
                 w.shared_expert_gate = layer.sh_gate_vec.data_ptr()
         self.weights = w
-        self._cfgs = {(pr, gv): make_config(s, per_row_mode=pr, gemv=gv)
+        self._cfgs = {(pr, gv): make_config(s, per_row_mode=pr, gemv=gv, t_layout=self.t_layout)
                       for pr in (False, True) for gv in (False, True)}
         self.cfg = self._cfgs[(False, False)]
         self.cfg_per_row = self._cfgs[(True, False)]
@@ -120,13 +135,24 @@ class DeviceLayer:
     def config(self, per_row_mode: bool = False, gemv: bool = False) -> N.MoeConfig:
         return self._cfgs[(bool(per_row_mode), bool(gemv))]
 
+    @staticmethod
+    def _to_t(m, count: int, n_out: int, k_in: int, stream: int):
+        """The t-layout copy of `count` stacked [n_out][k_in] NVFP4 matrices."""
+        pk = torch.empty((count, k_in, n_out // 2), dtype=torch.uint8, device=m.packed.device)
+        sc = torch.empty((count, k_in // 16, n_out), dtype=torch.uint8, device=m.packed.device)
+        N.moe_nvfp4_to_t_layout(m.packed.data_ptr(), m.scales.data_ptr(), count, n_out, k_in,
+                                pk.data_ptr(), sc.data_ptr(), stream)
+        shape = m.packed.shape[:-2]
+        return Nvfp4(pk.view(*shape, k_in, n_out // 2), sc.view(*shape, k_in // 16, n_out),
+                     m.scale2)
+
 
 class Workspace:
     """Caller-owned device workspace for one layer shape (zeroed once)."""
 
     def __init__(self, shape: MoeShape, device="cuda",
-                 stream: Optional[torch.cuda.Stream] = None):
-        self.nbytes = N.moe_workspace_size(make_config(shape))
+                 stream: Optional[torch.cuda.Stream] = None, t_layout: bool = False):
+        self.nbytes = N.moe_workspace_size(make_config(shape, t_layout=t_layout))
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
         N.moe_workspace_init(self.buf.data_ptr(), self.nbytes, _stream(stream))
 

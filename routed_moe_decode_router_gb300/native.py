@@ -17,6 +17,7 @@ MOE_MAX_ROWS = 32
 MOE_MAX_IDS = 256
 MOE_CHUNK_ROWS = 8
 MOE_CHUNK_IDS = 64
+MOE_STATIC_WORKSPACE_BYTES = 10 << 20
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 MOE_ROUTER_BF16, MOE_ROUTER_NVFP4 = 0, 1
 
@@ -44,7 +45,8 @@ class MoeConfig(C.Structure):
                 ("scoring", C.c_int), ("norm_topk_prob", C.c_int),
                 ("routed_scaling_factor", C.c_float), ("router_fmt", C.c_int),
                 ("has_shared", C.c_int), ("shared_gate", C.c_int),
-                ("per_row_mode", C.c_int), ("gemv_lever", C.c_int)]
+                ("per_row_mode", C.c_int), ("gemv_lever", C.c_int),
+                ("t_layout", C.c_int)]
 
 
 class ExpertTable(C.Structure):
@@ -73,7 +75,7 @@ class UnionTable(C.Structure):
 EXPORTS = ("moe_abi_version", "moe_last_error", "moe_check_config",
            "moe_workspace_size", "moe_workspace_init", "moe_route", "moe_union",
            "moe_forward", "moe_forward_timed", "moe_read_routing",
-           "moe_read_device_status", "moe_forward_static")
+           "moe_read_device_status", "moe_forward_static", "moe_nvfp4_to_t_layout")
 
 _lib = None
 _lock = threading.Lock()
@@ -115,6 +117,7 @@ def lib():
         L.moe_read_device_status.argtypes = [vp, sz, C.POINTER(C.c_int), vp]
         L.moe_forward_static.argtypes = [C.POINTER(MoeConfig), C.POINTER(MoeWeights),
                                          vp, vp, i, vp]
+        L.moe_nvfp4_to_t_layout.argtypes = [vp, vp, i, i, i, vp, vp, vp]
         for name in EXPORTS[2:]:
             if name != "moe_workspace_size":
                 getattr(L, name).restype = i
@@ -187,6 +190,14 @@ def moe_forward_static(cfg, w, x: int, out: int, rows: int, stream: int = 0):
     """moe_forward with the library's own static device workspace (for
     callers that cannot allocate device memory; see the header)."""
     _check(lib().moe_forward_static(C.byref(cfg), C.byref(w), x, out, rows, stream))
+
+
+def moe_nvfp4_to_t_layout(packed: int, scales: int, count: int, n_out: int, k_in: int,
+                          packed_t: int, scales_t: int, stream: int = 0):
+    """Convert `count` stacked NVFP4 [n_out][k_in] matrices to the t layout
+    (see the header)."""
+    _check(lib().moe_nvfp4_to_t_layout(packed, scales, count, n_out, k_in, packed_t,
+                                       scales_t, stream))
 
 
 def moe_read_device_status(ws: int, ws_bytes: int, stream: int = 0) -> int:

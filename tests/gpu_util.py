@@ -32,9 +32,9 @@ OUT_MAX_ABS = 3e-2
 NTHREADS = max(1, min(16, os.cpu_count() or 1))
 
 
-def gpu_run(weights, x, per_row=False, ws=None, dl=None, gemv=False):
-    dl = dl or L.DeviceLayer(weights)
-    ws = ws or L.Workspace(weights.shape)
+def gpu_run(weights, x, per_row=False, ws=None, dl=None, gemv=False, t_layout=False):
+    dl = dl or L.DeviceLayer(weights, t_layout=t_layout)
+    ws = ws or L.Workspace(weights.shape, t_layout=dl.t_layout)
     rows = x.shape[0]
     out = L.forward(dl, x, ws, per_row_mode=per_row, gemv=gemv)
     ids, wts, uni = L.read_routing(dl, ws, rows, per_row_mode=per_row)

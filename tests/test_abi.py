@@ -30,7 +30,7 @@ def header_functions():
 
 def test_library_exports_every_declared_function(lib):
     declared = header_functions()
-    assert len(declared) == 12
+    assert len(declared) == 13
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB], capture_output=True,
                          text=True, check=True).stdout
     exported = set(re.findall(r"\sT\s(moe_\w+)", out))
@@ -41,7 +41,7 @@ def test_library_exports_every_declared_function(lib):
 
 
 def test_abi_version(lib):
-    assert N.moe_abi_version() == 2
+    assert N.moe_abi_version() == 3
 
 
 def test_ctypes_layout_matches_c_header(tmp_path):
@@ -90,6 +90,7 @@ def good_cfg(**kw):
     ("router_fmt", 3, N.MoeError),
     ("per_row_mode", 2, N.MoeError),
     ("gemv_lever", 2, N.MoeError),
+    ("t_layout", 2, N.MoeError),
 ])
 def test_config_refusals(lib, field, value, status):
     cfg = good_cfg(**{field: value})
@@ -122,6 +123,22 @@ def test_workspace_size_independent_of_rows_and_positive(lib):
     for name, wl in synth.WORKLOADS.items():
         n = N.moe_workspace_size(L.make_config(wl.shape))
         assert n > 0 and n % 256 == 0, name
+
+
+def test_t_layout_workspace_holds_one_partial_row_per_cta(lib):
+    """The t layout adds room for 256 CTAs' partial output rows (fp32)."""
+    for name, wl in synth.WORKLOADS.items():
+        a = N.moe_workspace_size(L.make_config(wl.shape))
+        b = N.moe_workspace_size(L.make_config(wl.shape, t_layout=True))
+        assert b - a == 256 * wl.shape.hidden * 4, name
+
+
+def test_largest_config_fits_the_static_workspace(lib):
+    for t in (0, 1):
+        cfg = good_cfg(hidden=4096, num_experts=1024, router_width=1024, top_k=64,
+                       moe_inter=4096, shared_inter=4096, t_layout=t)
+        N.moe_check_config(cfg)
+        assert N.moe_workspace_size(cfg) <= N.MOE_STATIC_WORKSPACE_BYTES
 
 
 FAKE = 0x10000   # never dereferenced: every check below fails on the host
@@ -316,3 +333,29 @@ def test_python_helpers_refuse_host_memory_before_calling_the_library(monkeypatc
     with pytest.raises(ValueError, match="ids is on cpu"):
         L.union(None, dl.cfg, torch.zeros((2, 4), dtype=torch.int32), ws_cuda)
     assert called == []
+
+
+@pytest.mark.parametrize("case", ["count0", "n_not16", "k_not16", "k_big", "null",
+                                  "misaligned", "overlap"])
+def test_t_layout_conversion_refusals(lib, case):
+    """moe_nvfp4_to_t_layout refuses bad arguments on the host, before any
+    CUDA call."""
+    A, B, C_, D = 0x100000, 0x200000, 0x300000, 0x400000
+    args = dict(packed=A, scales=B, count=2, n_out=64, k_in=128, packed_t=C_, scales_t=D)
+    if case == "count0":
+        args["count"] = 0
+    elif case == "n_not16":
+        args["n_out"] = 40
+    elif case == "k_not16":
+        args["k_in"] = 72
+    elif case == "k_big":
+        args["k_in"] = 65536 + 16
+    elif case == "null":
+        args["scales_t"] = 0
+    elif case == "misaligned":
+        args["packed_t"] = C_ + 8
+    elif case == "overlap":
+        args["packed_t"] = A + 16
+    with pytest.raises(N.MoeError) as ei:
+        N.moe_nvfp4_to_t_layout(**args)
+    assert ei.value.status == 1

@@ -96,3 +96,23 @@ def test_full_size_graph_replay_matches_eager():
     for a, b in zip(eager, outs):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert ws.status() == 0
+
+
+@pytest.mark.parametrize("name,layer,rows", [("decode_h2048_e128", 0, 1),
+                                             ("decode_h2048_e128", 47, 1),
+                                             ("verify_h4096_e256", 3, 2),
+                                             ("sweep_h4096_e160", 7, 1),
+                                             ("prefill8_h2048_e512", 3, 1)])
+def test_full_size_t_layout_vs_oracle(name, layer, rows):
+    """Down projections in the t layout (the fused one-row form) at the
+    workloads' full sizes; union mode byte-identical to per-row mode."""
+    wl = synth.WORKLOADS[name]
+    weights = synth.make_layer(wl.shape, wl.seed_base + layer, device="cuda")
+    x = synth.make_rows(wl.shape, rows, seed=wl.seed_base + 500 + layer, device="cuda",
+                        corr=wl.corr)
+    dl = L.DeviceLayer(weights, t_layout=True)
+    res = G.gpu_run(weights, x, dl=dl)
+    st = G.check_parity(weights, x, res)
+    print(name, layer, rows, "t layout", st)
+    pr = G.gpu_run(weights, x, per_row=True, dl=dl)
+    assert torch.equal(res["out"].view(torch.int16), pr["out"].view(torch.int16))

@@ -311,6 +311,23 @@ def test_gemv_lever_ignored_above_one_row():
     assert torch.equal(a["out"].view(torch.int16), b["out"].view(torch.int16))
 
 
+def test_gemv_lever_applies_to_a_one_row_last_sub_chunk():
+    """gemv_lever is taken per sub-chunk: in a 9-row call at top_k 8 (8-row
+    sub-chunks) the first eight rows have the tensor-core bytes and the ninth
+    row, a sub-chunk of its own, the bytes of a one-row GEMV call."""
+    shape = PREFILL_SHAPES["k8"]
+    weights, x = G.make_case(shape, 9, seed_w=65, seed_x=66, corr=0.4)
+    dl = L.DeviceLayer(weights)
+    lev = G.gpu_run(weights, x, dl=dl, gemv=True)
+    G.check_parity(weights, x, lev)
+    head = G.gpu_run(weights, x[:8].contiguous(), dl=dl)["out"]
+    tail = G.gpu_run(weights, x[8:].contiguous(), dl=dl, gemv=True)["out"]
+    tail_tc = G.gpu_run(weights, x[8:].contiguous(), dl=dl)["out"]
+    assert torch.equal(lev["out"][:8].view(torch.int16), head.view(torch.int16))
+    assert torch.equal(lev["out"][8:].view(torch.int16), tail.view(torch.int16))
+    assert not torch.equal(tail.view(torch.int16), tail_tc.view(torch.int16))
+
+
 PREFILL_SHAPES = {
     "k8": S(num_experts=40, top_k=8),
     "k4_sigmoid": S(num_experts=64, top_k=4, moe_inter=256, shared_inter=256,
