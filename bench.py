@@ -17,11 +17,14 @@ on one GPU), the timed region is bracketed by barriers and the slowest rank's
 time is reported.  --impl reference times the CPU oracle on the same
 workload (rank 0 only).
 
-The default line is the single-row decode workload (48 layers).  Beside it,
-under "rows_1_to_8", the same measurement (µs per layer-step, mean union,
-roofline fraction of the kernel alone and of the graph step) for the full
-sweep at one and eight rows and for the eight-row prefill sub-chunk with
-independent and with correlated rows.  The CPU-baseline leg times the oracle
+The default line is the single-row decode workload (48 layers) with its down
+projections in the t layout (the fused one-row form; --down-layout picks the
+layout, "auto" = t for one-row workloads).  Beside it, under "rows_1_to_8",
+the same measurement (µs per layer-step, mean union, roofline fraction of
+the kernel alone and of the graph step) for the decode workload with
+output-major down projections, for the full sweep at one and eight rows and
+for the eight-row prefill sub-chunk with independent and with correlated
+rows.  The CPU-baseline leg times the oracle
 on all host cores and on one, and compares its outputs for the first and
 last timed layers of each workload with the GPU's (the "parity" verdicts).
 """
@@ -140,12 +143,13 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str, workload: str, rows: int):
+def committed_traffic(kernel: str, workload: str, rows: int, t_layout: bool = False):
     """DRAM bytes per launch of `kernel` from a committed ncu summary under
-    profiles/, if it was taken on the current kernel sources (else None)."""
+    profiles/, if it was taken on the current kernel sources (else None).
+    Lines of the t layout carry "layout=t" after the row count."""
     src = kernel_source_hash()
     pat = re.compile(r"bench-traffic:\s*kernel=(\S+)\s+workload=(\S+)\s+rows=(\d+)\s+"
-                     r"bytes_per_launch=(\d+)\s+src=(\w+)")
+                     r"(?:layout=(\w+)\s+)?bytes_per_launch=(\d+)\s+src=(\w+)")
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -156,8 +160,9 @@ def committed_traffic(kernel: str, workload: str, rows: int):
             for line in f:
                 m = pat.search(line)
                 if (m and m.group(1) == kernel and m.group(2) == workload
-                        and int(m.group(3)) == rows and m.group(5) == src):
-                    return int(m.group(4))
+                        and int(m.group(3)) == rows and (m.group(4) == "t") == t_layout
+                        and m.group(6) == src):
+                    return int(m.group(5))
     return None
 
 
@@ -372,16 +377,22 @@ def time_kernels(layers, xbuf, outbuf, ws, rows, steps, stream, gemv=False):
 # prefill sub-chunk with independent and with correlated rows.  Fewer layers
 # than the full stacks, each still far more distinct weight bytes per step
 # than the 129 MB L2.
+# (workload, rows, layers, activations of another workload or None, t layout)
 EXTRA_CONFIGS = [
-    ("sweep_h4096_e160", 1, 16, None),
-    ("sweep_h4096_e160", 8, 16, None),
-    ("prefill8_h2048_e512", 8, 16, None),
-    ("prefill8_h2048_e512", 8, 16, "verify_h4096_e256"),
+    ("decode_h2048_e128", 1, 48, None, False),
+    ("sweep_h4096_e160", 1, 16, None, True),
+    ("sweep_h4096_e160", 8, 16, None, False),
+    ("prefill8_h2048_e512", 8, 16, None, False),
+    ("prefill8_h2048_e512", 8, 16, "verify_h4096_e256", False),
 ]
 
 
-def measure_extra(name, rows, n_layers, corr_from, steps, warmup, dev, stream, peak, nthreads,
-                  with_parity):
+def use_t_layout(choice: str, rows: int) -> bool:
+    return choice == "t" or (choice == "auto" and rows == 1)
+
+
+def measure_extra(name, rows, n_layers, corr_from, t_layout, steps, warmup, dev, stream, peak,
+                  nthreads, with_parity):
     """µs per layer-step, mean union, roofline fractions (kernel alone and
     graph step) and, on rank 0, the parity verdict of one extra workload."""
     import torch
@@ -389,19 +400,20 @@ def measure_extra(name, rows, n_layers, corr_from, steps, warmup, dev, stream, p
     from routed_moe_decode_router_gb300 import synth
     wl = synth.WORKLOADS[name]
     corr = wl.corr if corr_from is None else synth.WORKLOADS[corr_from].corr
-    layers = [L.DeviceLayer(synth.make_layer(wl.shape, wl.seed_base + l, device=dev), device=dev)
-              for l in range(n_layers)]
+    layers = [L.DeviceLayer(synth.make_layer(wl.shape, wl.seed_base + l, device=dev), device=dev,
+                            t_layout=t_layout) for l in range(n_layers)]
     xbuf = torch.empty((n_layers, rows, wl.shape.hidden), dtype=torch.bfloat16, device=dev)
     for l in range(n_layers):
         xbuf[l] = synth.make_rows(wl.shape, rows, seed=wl.seed_base + 500 + l, device=dev,
                                   corr=corr)
     outbuf = torch.empty_like(xbuf)
-    ws = L.Workspace(wl.shape, device=dev)
+    ws = L.Workspace(wl.shape, device=dev, t_layout=t_layout)
     _, ms, U = time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream)
     us = ms * 1000.0 / (steps * n_layers)
     kern_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(steps, 10)), stream)
     bytes_per_layer = sum(layer_bytes(wl.shape, rows, u) for u in U) / n_layers
     out = {"workload": name, "rows": rows, "layers": n_layers,
+           "down_layout": "t (input-major)" if t_layout else "output-major",
            "activations": "independent N(0,1)" if corr is None
            else "correlated rows, a=%.3f" % corr,
            "us_per_layer_step": round(us, 3), "union_mean": round(sum(U) / len(U), 3),
@@ -409,7 +421,7 @@ def measure_extra(name, rows, n_layers, corr_from, steps, warmup, dev, stream, p
            "kernel_us": round(kern_ms * 1000.0, 3),
            "roofline_frac_kernel": round(bytes_per_layer / (kern_ms * 1e-3) / 1e9 / peak, 4),
            "roofline_frac_graph": round(bytes_per_layer / (us * 1e-6) / 1e9 / peak, 4),
-           "traffic": committed_traffic("moe_layer_kernel", name, rows)}
+           "traffic": committed_traffic("moe_layer_kernel", name, rows, t_layout)}
     if with_parity:
         from oracle import oracle
         oracle.build()
@@ -435,10 +447,10 @@ def run_ours(args, rank, world, local):
     wl0 = synth.WORKLOADS[args.workload]
     rows = args.rows or max(wl0.rows)
     n_layers = args.layers or wl0.layers
-    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev,
-                                                     args.t_layout)
+    t_layout = use_t_layout(args.down_layout, rows)
+    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev, t_layout)
     from routed_moe_decode_router_gb300 import layer as L
-    ws = L.Workspace(shape, device=dev, t_layout=args.t_layout)
+    ws = L.Workspace(shape, device=dev, t_layout=t_layout)
     stream = torch.cuda.Stream(device=dev)
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else
@@ -457,7 +469,7 @@ def run_ours(args, rank, world, local):
     step_bytes = sum(layer_bytes(shape, rows, u) for u in U)
     peak, peak_kind = hbm_peak()
     achieved = step_bytes / n_layers / (kernel_ms * 1e-3) / 1e9
-    traffic = committed_traffic("moe_layer_kernel", args.workload, rows)
+    traffic = committed_traffic("moe_layer_kernel", args.workload, rows, t_layout)
 
     # end to end through the public API with host buffers
     x_host = xbuf.cpu().pin_memory()
@@ -488,7 +500,7 @@ def run_ours(args, rank, world, local):
         "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, bf16 activations)",
         "config": workload_config(wl, shape, rows, n_layers, {
             "gemv_lever": int(args.gemv and rows == 1),
-            "down_layout": "t (input-major)" if args.t_layout else "output-major",
+            "down_layout": "t (input-major)" if t_layout else "output-major",
             "union_mean": round(sum(U) / len(U), 3),
             "l2": "no flush: each step streams %.2f GB of distinct weights (L2 129 MB)"
                   % (step_bytes / 1e9),
@@ -523,9 +535,9 @@ def run_ours(args, rank, world, local):
     if not args.no_extra and args.workload == "decode_h2048_e128" and not args.rows \
             and not args.layers:
         line["rows_1_to_8"] = [
-            measure_extra(name, r, nl, cf, args.steps, args.warmup, dev, stream, peak,
+            measure_extra(name, r, nl, cf, tl, args.steps, args.warmup, dev, stream, peak,
                           os.cpu_count() or 1, do_cpu)
-            for name, r, nl, cf in EXTRA_CONFIGS]
+            for name, r, nl, cf, tl in EXTRA_CONFIGS]
     return line
 
 
@@ -600,8 +612,9 @@ def main(argv=None):
     ap.add_argument("--cpu-1core-s", type=float, default=5.0)
     ap.add_argument("--gemv", action="store_true",
                     help="one-row layers on the CUDA-core GEMV variant (gemv_lever = 1)")
-    ap.add_argument("--t-layout", action="store_true",
-                    help="down projections in the t layout (the fused one-row form)")
+    ap.add_argument("--down-layout", choices=["auto", "t", "output"], default="auto",
+                    help="down projections in the t layout (the fused one-row form) or "
+                         "output-major; auto = t for one-row workloads")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the extra rows=1..8 workloads beside the headline line")
     ap.add_argument("--reference-budget-s", type=float, default=150.0)

@@ -409,9 +409,10 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     while (S > 2 && layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget) --S;
     if (layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget || (tl && S < 4))
         return fail(MOE_ERR_UNSUPPORTED, "stage ring does not fit in shared memory");
-    if (tl && di->sms > kMaxTCtas)
-        return fail(MOE_ERR_UNSUPPORTED, "t layout: %d SMs, the workspace holds partials of %d",
-                    di->sms, kMaxTCtas);
+    if (tl && (di->sms > kMaxTCtas || cfg->hidden > 256 * di->sms))
+        return fail(MOE_ERR_UNSUPPORTED,
+                    "t layout: %d SMs (the workspace holds the partials of at most %d, and "
+                    "each SM sums at most 256 outputs)", di->sms, kMaxTCtas);
     lp.stages = S;
     const int mc_gu = (cfg->hidden / kChunk + kConsumerWarps - 1) / kConsumerWarps;
     const int mc_d = lp.down_split ? L.inter_max / kChunk / 4

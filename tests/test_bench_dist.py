@@ -156,12 +156,15 @@ def test_committed_traffic_keyed_to_kernel_workload_rows_and_sources(tmp_path, m
     (tmp_path / "profiles").mkdir()
     (tmp_path / "profiles" / "k.md").write_text(
         "text\nbench-traffic: kernel=moe_layer_kernel workload=decode_h2048_e128 rows=1 "
-        "bytes_per_launch=24182016 src=abc123\n")
+        "bytes_per_launch=24182016 src=abc123\n"
+        "bench-traffic: kernel=moe_layer_kernel workload=decode_h2048_e128 rows=1 layout=t "
+        "bytes_per_launch=24100000 src=abc123\n")
     (tmp_path / "profiles" / "raw.ncu-rep").write_text(
         "bench-traffic: kernel=moe_layer_kernel workload=w rows=1 bytes_per_launch=1 src=abc123\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc123")
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1) == 24182016
+    assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1, True) == 24100000
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 8) is None
     assert bench.committed_traffic("moe_layer_kernel", "prefill8_h2048_e512", 1) is None
     assert bench.committed_traffic("moe_route_kernel", "decode_h2048_e128", 1) is None
