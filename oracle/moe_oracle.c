@@ -28,6 +28,14 @@
  *     [N][K/16], one per 16 contiguous inputs; one fp32 scale2 per matrix.
  *     A weight is (float)e2m1 * (float)e4m3 * scale2 evaluated in fp32 (the
  *     first product is exact, the multiply by scale2 rounds once).
+ *   - FP8 and BF16 experts (the other expert formats page
+ *     "forward_token_major.rs" names; it routes them to another path and
+ *     gives neither layout): FP8 matrix [N][K] = one E4M3 code per weight,
+ *     row-major, and one fp32 scale2 per matrix; BF16 matrix [N][K] = one
+ *     bfloat16 per weight, row-major, little-endian, times scale2.  A weight
+ *     is (float)decode(code) * scale2 in fp32 (one rounding).  The router,
+ *     the shared-expert gate vector and everything after the projections are
+ *     the same for every expert format.
  *   - top-k order: selection key descending, ties to the lower expert id.
  *     The selection decision is taken on keys rounded to fp32, the precision
  *     of the CUDA kernel's logits; softmax selects on the logit itself
@@ -111,14 +119,18 @@ uint16_t orc_round_bf16(double v)
     return sign | (uint16_t)(u >> 16);
 }
 
+/* Expert (or router) matrix formats. */
+enum { ORC_FMT_NVFP4 = 0, ORC_FMT_FP8 = 1, ORC_FMT_BF16 = 2 };
+
 typedef struct {
-    const uint8_t *packed; /* [N][K/2] */
-    const uint8_t *scales; /* [N][K/16] */
+    const uint8_t *packed; /* NVFP4 [N][K/2]; FP8 [N][K]; BF16 [N][2K] bytes */
+    const uint8_t *scales; /* NVFP4 [N][K/16]; unused by FP8 and BF16 */
     float scale2;
-} orc_fp4mat;
+    int fmt;               /* ORC_FMT_* */
+} orc_mat;
 
 /* Dequantised weight [n][k] of an NVFP4 matrix with K inputs, as fp32. */
-float orc_nvfp4_elem(const orc_fp4mat *m, int K, int n, int k)
+float orc_nvfp4_elem(const orc_mat *m, int K, int n, int k)
 {
     uint8_t byte = m->packed[(size_t)n * (size_t)(K / 2) + (size_t)(k / 2)];
     int code = (k & 1) ? (byte >> 4) : (byte & 15);
@@ -128,11 +140,27 @@ float orc_nvfp4_elem(const orc_fp4mat *m, int K, int n, int k)
     return qs * m->scale2;
 }
 
-/* Row n of an NVFP4 matrix, dequantised to fp64 (from the fp32 weights). */
-static void nvfp4_row(const orc_fp4mat *m, int K, int n, double *row)
+/* Dequantised weight [n][k] of a matrix of any format, as fp32. */
+float orc_mat_elem(const orc_mat *m, int K, int n, int k)
+{
+    const size_t i = (size_t)n * (size_t)K + (size_t)k;
+    if (m->fmt == ORC_FMT_FP8) {
+        float q = (float)orc_e4m3(m->packed[i]);
+        return q * m->scale2;
+    }
+    if (m->fmt == ORC_FMT_BF16) {
+        uint16_t bits = (uint16_t)(m->packed[2 * i] | ((unsigned)m->packed[2 * i + 1] << 8));
+        float q = (float)orc_bf16(bits);
+        return q * m->scale2;
+    }
+    return orc_nvfp4_elem(m, K, n, k);
+}
+
+/* Row n of a matrix, dequantised to fp64 (from the fp32 weights). */
+static void mat_row(const orc_mat *m, int K, int n, double *row)
 {
     for (int k = 0; k < K; ++k)
-        row[k] = (double)orc_nvfp4_elem(m, K, n, k);
+        row[k] = (double)orc_mat_elem(m, K, n, k);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -155,14 +183,14 @@ typedef struct {
 
 typedef struct {
     const uint16_t *router_bf16;  /* [E][H] */
-    orc_fp4mat router_fp4;        /* [E][H] */
+    orc_mat router_fp4;        /* [E][H] */
     const float *bias;            /* [E], sigmoid scoring */
-    const orc_fp4mat *gate;       /* [E] descriptors, each [I][H] */
-    const orc_fp4mat *up;         /* [E] descriptors, each [I][H] */
-    const orc_fp4mat *down;       /* [E] descriptors, each [H][I] */
-    orc_fp4mat sh_gate;           /* [Is][H] */
-    orc_fp4mat sh_up;             /* [Is][H] */
-    orc_fp4mat sh_down;           /* [H][Is] */
+    const orc_mat *gate;       /* [E] descriptors, each [I][H] */
+    const orc_mat *up;         /* [E] descriptors, each [I][H] */
+    const orc_mat *down;       /* [E] descriptors, each [H][I] */
+    orc_mat sh_gate;           /* [Is][H] */
+    orc_mat sh_up;             /* [Is][H] */
+    orc_mat sh_down;           /* [H][Is] */
     const uint16_t *sh_gate_vec;  /* [H] bf16 shared_expert_gate */
 } orc_weights;
 
@@ -184,7 +212,7 @@ void orc_router_logits(const orc_cfg *c, const orc_weights *w,
             xr[h] = orc_bf16(x[(size_t)r * H + h]);
         for (int e = 0; e < E; ++e) {
             if (c->router_nvfp4)
-                nvfp4_row(&w->router_fp4, H, e, wr);
+                mat_row(&w->router_fp4, H, e, wr);
             else
                 for (int h = 0; h < H; ++h)
                     wr[h] = orc_bf16(w->router_bf16[(size_t)e * H + h]);
@@ -320,23 +348,23 @@ static double silu64(double z) { return z / (1.0 + exp(-z)); }
  * (forward_token_major.rs: moe_expert_gate_up_shared_prefill, then
  * moe_expert_silu_down_shared_prefill, with the packed / scale / scale2
  * triplet of every expert matrix). */
-void orc_expert_mlp(int H, int I, const orc_fp4mat *g, const orc_fp4mat *u,
-                    const orc_fp4mat *d, const double *x, double *y)
+void orc_expert_mlp(int H, int I, const orc_mat *g, const orc_mat *u,
+                    const orc_mat *d, const double *x, double *y)
 {
     double *hbuf = malloc(sizeof(double) * (size_t)I);
     double *row = malloc(sizeof(double) * (size_t)(H > I ? H : I));
     for (int i = 0; i < I; ++i) {
         double gs = 0.0, us = 0.0;
-        nvfp4_row(g, H, i, row);
+        mat_row(g, H, i, row);
         for (int h = 0; h < H; ++h)
             gs += row[h] * x[h];
-        nvfp4_row(u, H, i, row);
+        mat_row(u, H, i, row);
         for (int h = 0; h < H; ++h)
             us += row[h] * x[h];
         hbuf[i] = silu64(gs) * us;
     }
     for (int o = 0; o < H; ++o) {
-        nvfp4_row(d, I, o, row);
+        mat_row(d, I, o, row);
         double acc = 0.0;
         for (int i = 0; i < I; ++i)
             acc += row[i] * hbuf[i];

@@ -38,9 +38,13 @@ def build(force: bool = False) -> str:
         return _SO
 
 
-class Fp4Mat(C.Structure):
+FMT = {"nvfp4": 0, "fp8": 1, "bf16": 2}
+
+
+class Mat(C.Structure):
+    """orc_mat: one matrix of any of the formats (FMT)."""
     _fields_ = [("packed", C.c_void_p), ("scales", C.c_void_p),
-                ("scale2", C.c_float)]
+                ("scale2", C.c_float), ("fmt", C.c_int)]
 
 
 class Cfg(C.Structure):
@@ -54,10 +58,10 @@ class Cfg(C.Structure):
 
 
 class Weights(C.Structure):
-    _fields_ = [("router_bf16", C.c_void_p), ("router_fp4", Fp4Mat),
+    _fields_ = [("router_bf16", C.c_void_p), ("router_fp4", Mat),
                 ("bias", C.c_void_p), ("gate", C.c_void_p),
                 ("up", C.c_void_p), ("down", C.c_void_p),
-                ("sh_gate", Fp4Mat), ("sh_up", Fp4Mat), ("sh_down", Fp4Mat),
+                ("sh_gate", Mat), ("sh_up", Mat), ("sh_down", Mat),
                 ("sh_gate_vec", C.c_void_p)]
 
 
@@ -75,8 +79,10 @@ def lib():
         L.orc_round_bf16.restype = C.c_uint16
         L.orc_round_bf16.argtypes = [C.c_double]
         L.orc_nvfp4_elem.restype = C.c_float
-        L.orc_nvfp4_elem.argtypes = [C.POINTER(Fp4Mat), C.c_int, C.c_int,
+        L.orc_nvfp4_elem.argtypes = [C.POINTER(Mat), C.c_int, C.c_int,
                                      C.c_int]
+        L.orc_mat_elem.restype = C.c_float
+        L.orc_mat_elem.argtypes = [C.POINTER(Mat), C.c_int, C.c_int, C.c_int]
         L.orc_router_logits.argtypes = [C.POINTER(Cfg), C.POINTER(Weights),
                                         C.c_void_p, C.c_int, C.c_void_p]
         L.orc_topk.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p]
@@ -87,8 +93,8 @@ def lib():
         L.orc_union.restype = C.c_int
         L.orc_union.argtypes = [C.c_void_p, C.c_int, C.c_int, C.c_void_p,
                                 C.c_void_p, C.c_void_p]
-        L.orc_expert_mlp.argtypes = [C.c_int, C.c_int, C.POINTER(Fp4Mat),
-                                     C.POINTER(Fp4Mat), C.POINTER(Fp4Mat),
+        L.orc_expert_mlp.argtypes = [C.c_int, C.c_int, C.POINTER(Mat),
+                                     C.POINTER(Mat), C.POINTER(Mat),
                                      C.c_void_p, C.c_void_p]
         L.orc_forward.argtypes = [C.POINTER(Cfg), C.POINTER(Weights),
                                   C.c_void_p, C.c_int, C.c_int, C.c_void_p,
@@ -143,23 +149,34 @@ def round_bf16(v: float) -> int:
 
 
 class HostMat:
-    """One NVFP4 matrix held in host memory for the oracle."""
+    """One matrix held in host memory for the oracle: NVFP4 (packed [N][K/2]
+    codes, scales [N][K/16]), FP8 (packed [N][K] E4M3 codes) or BF16 (packed
+    [N][2K] bytes, little-endian bfloat16); scale2 one fp32 per matrix."""
 
-    def __init__(self, packed, scales, scale2):
+    def __init__(self, packed, scales, scale2, fmt: str = "nvfp4"):
         self.packed = _np(packed).astype(np.uint8, copy=False)
-        self.scales = _np(scales).astype(np.uint8, copy=False)
+        self.fmt = fmt
         self.scale2 = float(np.asarray(_np(scale2)).reshape(()))
-        self.N, half = self.packed.shape
-        self.K = 2 * half
-        assert self.scales.shape == (self.N, self.K // 16)
+        self.N, width = self.packed.shape
+        self.K = {"nvfp4": 2 * width, "fp8": width, "bf16": width // 2}[fmt]
+        if fmt == "nvfp4":
+            self.scales = _np(scales).astype(np.uint8, copy=False)
+            assert self.scales.shape == (self.N, self.K // 16)
+        else:
+            self.scales = np.zeros(1, dtype=np.uint8)   # not read
 
-    def c(self) -> Fp4Mat:
-        return Fp4Mat(_ptr(self.packed), _ptr(self.scales), self.scale2)
+    def c(self) -> Mat:
+        return Mat(_ptr(self.packed), _ptr(self.scales), self.scale2, FMT[self.fmt])
 
 
 def nvfp4_elem(m: HostMat, n: int, k: int) -> float:
     cm = m.c()
     return lib().orc_nvfp4_elem(C.byref(cm), m.K, n, k)
+
+
+def mat_elem(m: HostMat, n: int, k: int) -> float:
+    cm = m.c()
+    return lib().orc_mat_elem(C.byref(cm), m.K, n, k)
 
 
 def topk(keys, k: int) -> np.ndarray:
@@ -230,11 +247,11 @@ class OracleLayer:
         sel = range(E) if experts is None else sorted(self._subset)
         arrs = {}
         for name in ("gate", "up", "down"):
-            arr = (Fp4Mat * E)()
+            arr = (Mat * E)()
             src = getattr(layer, name)
             s2 = _np(src.scale2).astype(np.float32)
             for e in sel:
-                hm = HostMat(src.packed[e], src.scales[e], s2[e])
+                hm = HostMat(src.packed[e], src.scales[e], s2[e], s.expert_fmt)
                 self._keep.append(hm)
                 arr[e] = hm.c()
             arrs[name] = arr
@@ -246,7 +263,7 @@ class OracleLayer:
             for name, field in (("sh_gate", "sh_gate"), ("sh_up", "sh_up"),
                                 ("sh_down", "sh_down")):
                 m = getattr(layer, name)
-                hm = HostMat(m.packed, m.scales, m.scale2)
+                hm = HostMat(m.packed, m.scales, m.scale2, s.expert_fmt)
                 self._keep.append(hm)
                 setattr(w, field, hm.c())
             self.sh_vec = _np(layer.sh_gate_vec)

@@ -1,9 +1,10 @@
 """Seeded synthetic inputs for the routed MoE layer.
 
 This module only draws random numbers and stores them in the layer's storage
-formats: bf16 activations and router weights, and NVFP4 expert matrices (FP4
-E2M1 codes, one FP8 E4M3 scale per 16 contiguous inputs, one fp32 scale per
-matrix).  It holds none of the layer's own arithmetic, and both the CUDA
+formats: bf16 activations and router weights, and the expert matrices in
+NVFP4 (FP4 E2M1 codes, one FP8 E4M3 scale per 16 contiguous inputs, one fp32
+scale per matrix), FP8 (one E4M3 code per weight, one fp32 scale per matrix)
+or BF16 (one bfloat16 per weight, scale 1).  It holds none of the layer's own arithmetic, and both the CUDA
 path and the CPU oracle read the bytes it writes.
 
 Every draw comes from a ``torch.Generator`` seeded per layer (weights) or per
@@ -58,6 +59,7 @@ class MoeShape:
     router_fmt: str = "bf16"          # "bf16" or "nvfp4"
     has_shared: bool = True
     shared_gated: bool = True
+    expert_fmt: str = "nvfp4"         # "nvfp4", "fp8" or "bf16" (routed and shared experts)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -97,9 +99,14 @@ WORKLOADS = {
 
 @dataclasses.dataclass
 class Nvfp4:
-    """One NVFP4 matrix [N][K] (or a stack [..., N, K] of them)."""
-    packed: torch.Tensor   # uint8 [..., N, K/2]; low nibble = even input
-    scales: torch.Tensor   # uint8 [..., N, K/16]; E4M3 bit patterns
+    """One expert matrix [N][K] (or a stack [..., N, K] of them).  NVFP4:
+    packed uint8 [..., N, K/2] (low nibble = even input), scales uint8
+    [..., N, K/16] (E4M3 bit patterns).  The other expert formats use the
+    same holder: FP8, packed uint8 [..., N, K] (E4M3 codes); BF16, packed
+    uint8 [..., N, 2K] (the little-endian bfloat16 bytes); both with empty
+    scales [..., N, 0]."""
+    packed: torch.Tensor
+    scales: torch.Tensor
     scale2: torch.Tensor   # float32 [...]; one per matrix
 
     def to(self, device) -> "Nvfp4":
@@ -180,6 +187,33 @@ def quantize_nvfp4(w: torch.Tensor) -> Nvfp4:
                  scale2.float().contiguous())
 
 
+def quantize_fp8(w: torch.Tensor) -> Nvfp4:
+    """Encode float weights [..., N, K] into FP8: scale2 = amax(|W|) / 448 per
+    matrix, each element the round-to-nearest-even E4M3 code of w / scale2."""
+    w = w.float()
+    *lead, N, K = w.shape
+    amax = w.abs().amax(dim=(-2, -1))
+    scale2 = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    v = (w / scale2.reshape(*lead, 1, 1)).clamp(-E4M3_MAX, E4M3_MAX)
+    codes = v.to(torch.float8_e4m3fn).view(torch.uint8)
+    return Nvfp4(codes.contiguous(),
+                 torch.zeros((*lead, N, 0), dtype=torch.uint8, device=w.device),
+                 scale2.float().contiguous())
+
+
+def store_bf16(w: torch.Tensor) -> Nvfp4:
+    """Store float weights [..., N, K] as bfloat16 (round to nearest even),
+    scale2 = 1."""
+    *lead, N, K = w.shape
+    b = w.float().to(torch.bfloat16).contiguous()
+    return Nvfp4(b.view(torch.uint8).reshape(*lead, N, 2 * K).contiguous(),
+                 torch.zeros((*lead, N, 0), dtype=torch.uint8, device=w.device),
+                 torch.ones(tuple(lead), dtype=torch.float32, device=w.device))
+
+
+ENCODERS = {"nvfp4": quantize_nvfp4, "fp8": quantize_fp8, "bf16": store_bf16}
+
+
 def _normal(gen, shape, std, device):
     return torch.randn(shape, generator=gen, device=device,
                        dtype=torch.float32) * std
@@ -188,7 +222,8 @@ def _normal(gen, shape, std, device):
 def make_layer(shape: MoeShape, seed: int, device="cpu",
                std: float = 0.02, router_only: bool = False) -> MoeLayerWeights:
     """Random-init weights of one routed MoE layer, N(0, std) everywhere,
-    experts quantised to NVFP4.  Draw order: router, correction bias (sigmoid
+    experts encoded in the shape's expert format (NVFP4, FP8 or BF16; the
+    same draws for every format).  Draw order: router, correction bias (sigmoid
     scoring only, U(-0.1, 0.1)), shared-expert gate vector, shared gate / up
     / down, then the routed experts in fixed-size chunks (gate, up, down per
     chunk).  ``router_only`` stops after the routing weights (router and
@@ -222,21 +257,22 @@ def make_layer(shape: MoeShape, seed: int, device="cpu",
                                None, None, None, None)
 
     sh_gate = sh_up = sh_down = sh_vec = None
+    enc = ENCODERS[s.expert_fmt]
     if s.has_shared:
         sh_vec = _normal(gen, (H,), std, device).to(torch.bfloat16)
-        sh_gate = quantize_nvfp4(_normal(gen, (Is, H), std, device))
-        sh_up = quantize_nvfp4(_normal(gen, (Is, H), std, device))
-        sh_down = quantize_nvfp4(_normal(gen, (H, Is), std, device))
+        sh_gate = enc(_normal(gen, (Is, H), std, device))
+        sh_up = enc(_normal(gen, (Is, H), std, device))
+        sh_down = enc(_normal(gen, (H, Is), std, device))
 
     chunk = max(1, min(E, (1 << 25) // (I * H)))
     gp, gs_, g2, up_, us, u2, dp, ds, d2 = ([] for _ in range(9))
     for e0 in range(0, E, chunk):
         c = min(chunk, E - e0)
-        q = quantize_nvfp4(_normal(gen, (c, I, H), std, device))
+        q = enc(_normal(gen, (c, I, H), std, device))
         gp.append(q.packed); gs_.append(q.scales); g2.append(q.scale2)
-        q = quantize_nvfp4(_normal(gen, (c, I, H), std, device))
+        q = enc(_normal(gen, (c, I, H), std, device))
         up_.append(q.packed); us.append(q.scales); u2.append(q.scale2)
-        q = quantize_nvfp4(_normal(gen, (c, H, I), std, device))
+        q = enc(_normal(gen, (c, H, I), std, device))
         dp.append(q.packed); ds.append(q.scales); d2.append(q.scale2)
     gate = Nvfp4(torch.cat(gp), torch.cat(gs_), torch.cat(g2))
     up = Nvfp4(torch.cat(up_), torch.cat(us), torch.cat(u2))

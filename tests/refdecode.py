@@ -65,3 +65,30 @@ def nvfp4_dense(packed, scales, scale2) -> np.ndarray:
     s = np.repeat(s, 16, axis=1)
     w = (q * s).astype(np.float32) * s2
     return w.astype(np.float32).astype(np.float64)
+
+
+def fp8_dense(packed, scale2) -> np.ndarray:
+    """One FP8 matrix [N][K] (E4M3 codes, one fp32 scale2): w = e4m3 * scale2
+    with the multiply rounded to float32."""
+    codes = to_np(packed).astype(np.uint8)
+    s2 = np.float32(np.asarray(to_np(scale2)).reshape(()))
+    q = e4m3_decode(codes).astype(np.float32)
+    return (q * s2).astype(np.float32).astype(np.float64)
+
+
+def bf16_dense(packed, scale2) -> np.ndarray:
+    """One BF16 matrix [N][K] stored as [N][2K] little-endian bytes, times
+    scale2 (float32 multiply)."""
+    b = to_np(packed).astype(np.uint8)
+    bits = np.ascontiguousarray(b).view("<u2")
+    s2 = np.float32(np.asarray(to_np(scale2)).reshape(()))
+    q = bf16_decode(bits).astype(np.float32)
+    return (q * s2).astype(np.float32).astype(np.float64)
+
+
+def expert_dense(fmt, packed, scales, scale2) -> np.ndarray:
+    if fmt == "fp8":
+        return fp8_dense(packed, scale2)
+    if fmt == "bf16":
+        return bf16_dense(packed, scale2)
+    return nvfp4_dense(packed, scales, scale2)

@@ -40,6 +40,14 @@ MUTANTS = [
      "(k & 1) ? (byte & 15) : (byte >> 4)"),
     ("scale_block_of_32", "(size_t)(k / 16)]", "(size_t)(k / 32)]"),
     ("scale2_dropped", "return qs * m->scale2;", "return qs;"),
+    # FP8 and BF16 expert matrices
+    ("fp8_scale2_dropped", "float q = (float)orc_e4m3(m->packed[i]);\n        return q * m->scale2;",
+     "float q = (float)orc_e4m3(m->packed[i]);\n        return q;"),
+    ("fp8_row_stride_halved", "const size_t i = (size_t)n * (size_t)K + (size_t)k;",
+     "const size_t i = (size_t)n * (size_t)(K / 2) + (size_t)k;"),
+    ("bf16_bytes_swapped", "(uint16_t)(m->packed[2 * i] | ((unsigned)m->packed[2 * i + 1] << 8))",
+     "(uint16_t)(m->packed[2 * i + 1] | ((unsigned)m->packed[2 * i] << 8))"),
+    ("bf16_read_as_fp8", "    if (m->fmt == ORC_FMT_FP8) {", "    if (m->fmt != ORC_FMT_NVFP4) {"),
     ("scale_row_stride_halved", "m->scales[(size_t)n * (size_t)(K / 16)",
      "m->scales[(size_t)n * (size_t)(K / 32)"),
     ("packed_row_stride_halved", "m->packed[(size_t)n * (size_t)(K / 2)",
@@ -52,8 +60,8 @@ MUTANTS = [
     ("router_dot_drops_last_input",
      "            for (int h = 0; h < H; ++h)\n                acc += xr[h] * wr[h];",
      "            for (int h = 0; h < H - 1; ++h)\n                acc += xr[h] * wr[h];"),
-    ("nvfp4_router_row0", "nvfp4_row(&w->router_fp4, H, e, wr);",
-     "nvfp4_row(&w->router_fp4, H, 0, wr);"),
+    ("nvfp4_router_row0", "mat_row(&w->router_fp4, H, e, wr);",
+     "mat_row(&w->router_fp4, H, 0, wr);"),
     # top-k and routing weights
     ("topk_ties_to_higher_id", "key[e] > key[best]", "key[e] >= key[best]"),
     ("topk_repeats_an_expert", "            if (taken[e])\n                continue;\n", ""),
@@ -91,12 +99,12 @@ MUTANTS = [
     # expert MLP
     ("silu_sign", "return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
     ("swiglu_operands_swapped", "hbuf[i] = silu64(gs) * us;", "hbuf[i] = gs * silu64(us);"),
-    ("up_reads_gate_matrix", "nvfp4_row(u, H, i, row);", "nvfp4_row(g, H, i, row);"),
+    ("up_reads_gate_matrix", "mat_row(u, H, i, row);", "mat_row(g, H, i, row);"),
     ("gate_dot_drops_last_input", "        for (int h = 0; h < H; ++h)\n            gs += row[h] * x[h];",
      "        for (int h = 0; h < H - 1; ++h)\n            gs += row[h] * x[h];"),
     ("down_dot_drops_last_input", "        for (int i = 0; i < I; ++i)\n            acc += row[i] * hbuf[i];",
      "        for (int i = 0; i < I - 1; ++i)\n            acc += row[i] * hbuf[i];"),
-    ("down_row_wraps_at_inner_size", "nvfp4_row(d, I, o, row);", "nvfp4_row(d, I, o % I, row);"),
+    ("down_row_wraps_at_inner_size", "mat_row(d, I, o, row);", "mat_row(d, I, o % I, row);"),
     # whole layer
     ("expert_ids_transposed", "int e = j->ids[(size_t)r * k + s];",
      "int e = j->ids[(size_t)s * j->rows + r];"),

@@ -106,6 +106,49 @@ def test_nvfp4_elem_vs_library_decode(orc):
     assert np.array_equal(got, want)
 
 
+def test_fp8_elem_vs_library_decode(orc):
+    """FP8 experts: one E4M3 code per weight, row-major, times scale2 (fp32)."""
+    rng = np.random.default_rng(4)
+    N, K = 24, 80
+    codes = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x41             # keep NaN codes out
+    s2 = np.float32(0.0371)
+    m = orc.HostMat(codes, None, s2, "fp8")
+    want = ref.fp8_dense(codes, s2)
+    got = np.array([[orc.mat_elem(m, n, k) for k in range(K)] for n in range(N)])
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("s2", [1.0, 0.73])
+def test_bf16_elem_vs_library_decode(orc, s2):
+    """BF16 experts: one little-endian bfloat16 per weight, row-major, times
+    scale2 (fp32)."""
+    rng = np.random.default_rng(5)
+    N, K = 16, 48
+    bits = rng.integers(0, 1 << 16, size=(N, K), dtype=np.uint32).astype(np.uint16)
+    bits[(bits & 0x7F80) == 0x7F80] &= 0xBFFF         # keep infinities and NaNs out
+    raw = bits.astype("<u2").view(np.uint8).reshape(N, 2 * K)
+    m = orc.HostMat(raw, None, np.float32(s2), "bf16")
+    want = ref.bf16_dense(raw, np.float32(s2))
+    got = np.array([[orc.mat_elem(m, n, k) for k in range(K)] for n in range(N)])
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "bf16"])
+def test_other_formats_roundtrip(orc, fmt):
+    """The FP8 encoder is within half an E4M3 step of the weights and the
+    BF16 one within half a bfloat16 step: what the oracle reads back is the
+    value the generator meant."""
+    g = torch.Generator().manual_seed(6)
+    w = torch.randn((8, 64), generator=g) * 0.02
+    q = synth.ENCODERS[fmt](w)
+    m = orc.HostMat(q.packed, q.scales, q.scale2, fmt)
+    deq = np.array([[orc.mat_elem(m, n, k) for k in range(64)] for n in range(8)])
+    err = np.abs(deq - w.double().numpy())
+    rel = 2.0 ** -4 if fmt == "fp8" else 2.0 ** -8
+    assert np.all(err <= rel * np.abs(w.double().numpy()) + 2.0 ** -9 * float(q.scale2))
+
+
 def test_quantizer_roundtrip_within_grid_step(orc):
     """dequant(quantize(W)) stays within one block step of W; a wrong nibble
     order or scale index would give errors of the size of W itself."""
@@ -142,12 +185,12 @@ def dense_mats(layer):
         d["router"] = ref.bf16_decode(ref.to_np(layer.router_bf16))
     for name in ("gate", "up", "down"):
         src = getattr(layer, name)
-        d[name] = [ref.nvfp4_dense(src.packed[e], src.scales[e], src.scale2[e])
+        d[name] = [ref.expert_dense(s.expert_fmt, src.packed[e], src.scales[e], src.scale2[e])
                    for e in range(s.num_experts)]
     if s.has_shared:
         for name in ("sh_gate", "sh_up", "sh_down"):
             m = getattr(layer, name)
-            d[name] = ref.nvfp4_dense(m.packed, m.scales, m.scale2)
+            d[name] = ref.expert_dense(s.expert_fmt, m.packed, m.scales, m.scale2)
         d["sh_vec"] = ref.bf16_decode(ref.to_np(layer.sh_gate_vec))
     return d
 
@@ -387,15 +430,16 @@ def test_union_mean_matches_independent_routing_closed_form(orc):
 # Expert MLP and the whole layer
 # ---------------------------------------------------------------------------
 
-def test_expert_mlp_vs_torch_swiglu(orc):
-    shape = small_shape()
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8", "bf16"])
+def test_expert_mlp_vs_torch_swiglu(orc, fmt):
+    shape = small_shape(expert_fmt=fmt)
     layer = synth.make_layer(shape, seed=17)
     d = dense_mats(layer)
     x = np.random.default_rng(18).standard_normal(shape.hidden)
     for e in (0, 5):
-        g = orc.HostMat(layer.gate.packed[e], layer.gate.scales[e], layer.gate.scale2[e])
-        u = orc.HostMat(layer.up.packed[e], layer.up.scales[e], layer.up.scale2[e])
-        dn = orc.HostMat(layer.down.packed[e], layer.down.scales[e], layer.down.scale2[e])
+        g = orc.HostMat(layer.gate.packed[e], layer.gate.scales[e], layer.gate.scale2[e], fmt)
+        u = orc.HostMat(layer.up.packed[e], layer.up.scales[e], layer.up.scale2[e], fmt)
+        dn = orc.HostMat(layer.down.packed[e], layer.down.scales[e], layer.down.scale2[e], fmt)
         y = orc.expert_mlp(g, u, dn, x)
         want = swiglu64(x, d["gate"][e], d["up"][e], d["down"][e])
         np.testing.assert_allclose(y, want, rtol=1e-11, atol=1e-14)
@@ -427,6 +471,10 @@ def test_forward_reduces_to_swiglu(orc):
     dict(shared_gated=False),
     dict(has_shared=False),
     dict(moe_inter=32, shared_inter=96),      # shared expert wider than the routed ones
+    dict(expert_fmt="fp8"),
+    dict(expert_fmt="bf16"),
+    dict(expert_fmt="fp8", scoring="sigmoid", routed_scaling_factor=2.5, router_fmt="nvfp4"),
+    dict(expert_fmt="bf16", shared_gated=False, norm_topk_prob=False),
 ])
 def test_forward_vs_dense_bruteforce(orc, variant):
     shape = small_shape(**variant)
