@@ -22,9 +22,9 @@ projections in the t layout (the fused one-row form; --down-layout picks the
 layout, "auto" = t for one-row workloads).  Beside it, under "rows_1_to_8",
 the same measurement (µs per layer-step, mean union, roofline fraction of
 the kernel alone and of the graph step) for the decode workload with
-output-major down projections, for the full sweep at one and eight rows and
-for the eight-row prefill sub-chunk with independent and with correlated
-rows.  The CPU-baseline leg times the oracle
+output-major down projections, for the full sweep at one and eight rows, for
+the eight-row prefill sub-chunk with independent and with correlated rows,
+and for the decode workload with FP8 and with BF16 expert matrices.  The CPU-baseline leg times the oracle
 on all host cores and on one, and compares its outputs for the first and
 last timed layers of each workload with the GPU's (the "parity" verdicts).
 """
@@ -107,9 +107,14 @@ def layer_bytes(shape, rows: int, U: int) -> int:
     down weights and scales once (+3 fp32 scale2), the shared expert, the
     router, the correction bias, the shared-expert gate vector, x and out."""
     H, E, I, Is = shape.hidden, shape.num_experts, shape.moe_inter, shape.shared_inter
-    b = U * (3 * nvfp4_bytes(I, H) + 12)
+    fmt = getattr(shape, "expert_fmt", "nvfp4")
+
+    def mat(n, k):   # one expert matrix in the expert format
+        return nvfp4_bytes(n, k) if fmt == "nvfp4" else n * k * (1 if fmt == "fp8" else 2)
+
+    b = U * (3 * mat(I, H) + 12)
     if shape.has_shared:
-        b += 3 * nvfp4_bytes(Is, H) + 12
+        b += 3 * mat(Is, H) + 12
         if shape.shared_gated:
             b += H * 2
     b += E * H * 2 if shape.router_fmt == "bf16" else nvfp4_bytes(E, H) + 4
@@ -143,13 +148,16 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(kernel: str, workload: str, rows: int, t_layout: bool = False):
+def committed_traffic(kernel: str, workload: str, rows: int, t_layout: bool = False,
+                      fmt: str = "nvfp4"):
     """DRAM bytes per launch of `kernel` from a committed ncu summary under
     profiles/, if it was taken on the current kernel sources (else None).
-    Lines of the t layout carry "layout=t" after the row count."""
+    Lines of the t layout carry "layout=t" after the row count, and lines of
+    FP8 or BF16 experts "fmt=fp8" / "fmt=bf16" after that."""
     src = kernel_source_hash()
     pat = re.compile(r"bench-traffic:\s*kernel=(\S+)\s+workload=(\S+)\s+rows=(\d+)\s+"
-                     r"(?:layout=(\w+)\s+)?bytes_per_launch=(\d+)\s+src=(\w+)")
+                     r"(?:layout=(\w+)\s+)?(?:fmt=(\w+)\s+)?bytes_per_launch=(\d+)\s+"
+                     r"src=(\w+)")
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -161,8 +169,8 @@ def committed_traffic(kernel: str, workload: str, rows: int, t_layout: bool = Fa
                 m = pat.search(line)
                 if (m and m.group(1) == kernel and m.group(2) == workload
                         and int(m.group(3)) == rows and (m.group(4) == "t") == t_layout
-                        and m.group(6) == src):
-                    return int(m.group(5))
+                        and (m.group(5) or "nvfp4") == fmt and m.group(7) == src):
+                    return int(m.group(6))
     return None
 
 
@@ -378,12 +386,16 @@ def time_kernels(layers, xbuf, outbuf, ws, rows, steps, stream, gemv=False):
 # than the full stacks, each still far more distinct weight bytes per step
 # than the 129 MB L2.
 # (workload, rows, layers, activations of another workload or None, t layout)
+# (workload, rows, layers, activations of another workload or None, t layout,
+# expert format)
 EXTRA_CONFIGS = [
-    ("decode_h2048_e128", 1, 48, None, False),
-    ("sweep_h4096_e160", 1, 16, None, True),
-    ("sweep_h4096_e160", 8, 16, None, False),
-    ("prefill8_h2048_e512", 8, 16, None, False),
-    ("prefill8_h2048_e512", 8, 16, "verify_h4096_e256", False),
+    ("decode_h2048_e128", 1, 48, None, False, "nvfp4"),
+    ("sweep_h4096_e160", 1, 16, None, True, "nvfp4"),
+    ("sweep_h4096_e160", 8, 16, None, False, "nvfp4"),
+    ("prefill8_h2048_e512", 8, 16, None, False, "nvfp4"),
+    ("prefill8_h2048_e512", 8, 16, "verify_h4096_e256", False, "nvfp4"),
+    ("decode_h2048_e128", 1, 48, None, False, "fp8"),
+    ("decode_h2048_e128", 1, 48, None, False, "bf16"),
 ]
 
 
@@ -391,29 +403,33 @@ def use_t_layout(choice: str, rows: int) -> bool:
     return choice == "t" or (choice == "auto" and rows == 1)
 
 
-def measure_extra(name, rows, n_layers, corr_from, t_layout, steps, warmup, dev, stream, peak,
-                  nthreads, with_parity):
+def measure_extra(name, rows, n_layers, corr_from, t_layout, fmt, steps, warmup, dev, stream,
+                  peak, nthreads, with_parity):
     """µs per layer-step, mean union, roofline fractions (kernel alone and
     graph step) and, on rank 0, the parity verdict of one extra workload."""
+    import dataclasses
+
     import torch
     from routed_moe_decode_router_gb300 import layer as L
     from routed_moe_decode_router_gb300 import synth
     wl = synth.WORKLOADS[name]
+    shape = dataclasses.replace(wl.shape, expert_fmt=fmt)
     corr = wl.corr if corr_from is None else synth.WORKLOADS[corr_from].corr
-    layers = [L.DeviceLayer(synth.make_layer(wl.shape, wl.seed_base + l, device=dev), device=dev,
+    layers = [L.DeviceLayer(synth.make_layer(shape, wl.seed_base + l, device=dev), device=dev,
                             t_layout=t_layout) for l in range(n_layers)]
-    xbuf = torch.empty((n_layers, rows, wl.shape.hidden), dtype=torch.bfloat16, device=dev)
+    xbuf = torch.empty((n_layers, rows, shape.hidden), dtype=torch.bfloat16, device=dev)
     for l in range(n_layers):
-        xbuf[l] = synth.make_rows(wl.shape, rows, seed=wl.seed_base + 500 + l, device=dev,
+        xbuf[l] = synth.make_rows(shape, rows, seed=wl.seed_base + 500 + l, device=dev,
                                   corr=corr)
     outbuf = torch.empty_like(xbuf)
-    ws = L.Workspace(wl.shape, device=dev, t_layout=t_layout)
+    ws = L.Workspace(shape, device=dev, t_layout=t_layout)
     _, ms, U = time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream)
     us = ms * 1000.0 / (steps * n_layers)
     kern_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(steps, 10)), stream)
-    bytes_per_layer = sum(layer_bytes(wl.shape, rows, u) for u in U) / n_layers
+    bytes_per_layer = sum(layer_bytes(shape, rows, u) for u in U) / n_layers
     out = {"workload": name, "rows": rows, "layers": n_layers,
            "down_layout": "t (input-major)" if t_layout else "output-major",
+           "expert_fmt": fmt,
            "activations": "independent N(0,1)" if corr is None
            else "correlated rows, a=%.3f" % corr,
            "us_per_layer_step": round(us, 3), "union_mean": round(sum(U) / len(U), 3),
@@ -421,7 +437,7 @@ def measure_extra(name, rows, n_layers, corr_from, t_layout, steps, warmup, dev,
            "kernel_us": round(kern_ms * 1000.0, 3),
            "roofline_frac_kernel": round(bytes_per_layer / (kern_ms * 1e-3) / 1e9 / peak, 4),
            "roofline_frac_graph": round(bytes_per_layer / (us * 1e-6) / 1e9 / peak, 4),
-           "traffic": committed_traffic("moe_layer_kernel", name, rows, t_layout)}
+           "traffic": committed_traffic("moe_layer_kernel", name, rows, t_layout, fmt)}
     if with_parity:
         from oracle import oracle
         oracle.build()
@@ -535,9 +551,9 @@ def run_ours(args, rank, world, local):
     if not args.no_extra and args.workload == "decode_h2048_e128" and not args.rows \
             and not args.layers:
         line["rows_1_to_8"] = [
-            measure_extra(name, r, nl, cf, tl, args.steps, args.warmup, dev, stream, peak,
+            measure_extra(name, r, nl, cf, tl, fmt, args.steps, args.warmup, dev, stream, peak,
                           os.cpu_count() or 1, do_cpu)
-            for name, r, nl, cf, tl in EXTRA_CONFIGS]
+            for name, r, nl, cf, tl, fmt in EXTRA_CONFIGS]
     return line
 
 

@@ -103,6 +103,20 @@ typedef enum moe_status {
 
 enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
 enum { MOE_ROUTER_BF16 = 0, MOE_ROUTER_NVFP4 = 1 };
+/* Expert matrix formats (moe_config.expert_fmt; routed and shared experts):
+ *   NVFP4: as described at the top of this file;
+ *   FP8:   packed uint8 [N][K], one E4M3 (bias 7, no infinity) code per
+ *          weight, row-major; scales not used (may be NULL); weight =
+ *          e4m3(code) * scale2;
+ *   BF16:  packed [N][K] bfloat16 (2 bytes per weight, little-endian),
+ *          row-major; scales not used (may be NULL); weight = bf16 * scale2.
+ * The forward_token_major.rs page names BF16 and FP8 experts as formats its
+ * token-major path hands to another path, without giving their layout; the
+ * layouts above are this library's reading.  A 16-row tile of an FP8 or
+ * BF16 matrix is 16*K or 32*K bytes: configurations whose gate/up or down
+ * tiles do not fit two shared-memory ring slots are refused at the first
+ * forward (MOE_ERR_UNSUPPORTED; BF16 at hidden 4096, for example). */
+enum { MOE_EXPERT_NVFP4 = 0, MOE_EXPERT_FP8 = 1, MOE_EXPERT_BF16 = 2 };
 
 /* One NVFP4 matrix whose pointers the host knows (router, shared expert). */
 typedef struct moe_nvfp4 {
@@ -158,11 +172,19 @@ typedef struct moe_config {
                                     every row as a sub-chunk of its own and
                                     runs the fused one-row form (see
                                     moe_forward).  Gate and up projections
-                                    keep the layout above either way. */
+                                    keep the layout above either way; NVFP4
+                                    experts only. */
+    int expert_fmt;              /* MOE_EXPERT_NVFP4, _FP8 or _BF16 (every
+                                    routed and shared expert matrix; the
+                                    router has its own router_fmt).
+                                    gemv_lever applies to NVFP4 experts
+                                    only; the other formats ignore it. */
 } moe_config;
 
-/* Per-expert NVFP4 matrices: device arrays indexed by expert id
- * (forward_token_major.rs: packed_ptrs / scale_ptrs / scale2_vals). */
+/* Per-expert matrices (in the config's expert_fmt): device arrays indexed by
+ * expert id (forward_token_major.rs: packed_ptrs / scale_ptrs / scale2_vals).
+ * FP8 and BF16 experts leave `scales` unused (it may be NULL).  moe_nvfp4
+ * likewise describes a shared-expert matrix of any expert format. */
 typedef struct moe_expert_table {
     const uint8_t *const *packed;  /* device array [E] of device pointers */
     const uint8_t *const *scales;  /* device array [E] of device pointers */

@@ -16,7 +16,7 @@ namespace moe {
 cudaError_t launch_route(const RouteParams &p, cudaStream_t stream);
 cudaError_t launch_union(const UnionParams &p, cudaStream_t stream);
 cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
-                         bool gemv, bool t_layout, cudaStream_t stream);
+                         bool gemv, bool t_layout, int expert_fmt, cudaStream_t stream);
 cudaError_t launch_t_layout(const uint8_t *packed, const uint8_t *scales, int count, int n_out,
                             int k_in, uint8_t *packed_t, uint8_t *scales_t, cudaStream_t stream);
 cudaError_t set_layer_smem_limit(int bytes);
@@ -116,6 +116,12 @@ moe_status check_cfg(const moe_config *c) {
     if ((c->norm_topk_prob | c->shared_gate | c->per_row_mode | c->gemv_lever | c->t_layout) & ~1)
         return fail(MOE_ERR_INVALID_ARG,
                     "norm_topk_prob, shared_gate, per_row_mode, gemv_lever, t_layout are 0/1");
+    if (c->expert_fmt != MOE_EXPERT_NVFP4 && c->expert_fmt != MOE_EXPERT_FP8 &&
+        c->expert_fmt != MOE_EXPERT_BF16)
+        return fail(MOE_ERR_INVALID_ARG, "expert_fmt=%d: must be nvfp4 (0), fp8 (1) or bf16 (2)",
+                    c->expert_fmt);
+    if (c->t_layout && c->expert_fmt != MOE_EXPERT_NVFP4)
+        return fail(MOE_ERR_UNSUPPORTED, "the t layout holds NVFP4 down projections only");
     return MOE_OK;
 }
 
@@ -143,6 +149,7 @@ UnionParams union_params(const moe_config *c, const moe_weights *w, const int32_
     p.per_row_mode = c->per_row_mode;
     p.has_tables = w != nullptr;
     p.has_shared = c->has_shared;
+    p.has_scales = c->expert_fmt == MOE_EXPERT_NVFP4;
     p.ids = ids;
     if (w) {
         p.gate = w->gate;
@@ -166,17 +173,20 @@ moe_status check_ws(const moe_config *c, const void *ws, size_t ws_bytes, WsLayo
     return MOE_OK;
 }
 
-moe_status check_mat(const moe_nvfp4 &m, const char *name) {
-    if (!m.packed || !m.scales) return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer", name);
-    if (!aligned(m.packed, 16) || !aligned(m.scales, 16))
+// has_scales = 0 (FP8 and BF16 experts): the scales pointers are not read
+// and may be NULL.
+moe_status check_mat(const moe_nvfp4 &m, const char *name, bool has_scales = true) {
+    if (!m.packed || (has_scales && !m.scales))
+        return fail(MOE_ERR_INVALID_ARG, "%s: NULL pointer", name);
+    if (!aligned(m.packed, 16) || (has_scales && !aligned(m.scales, 16)))
         return fail(MOE_ERR_INVALID_ARG, "%s: packed/scales must be 16-byte aligned", name);
     return MOE_OK;
 }
 
-moe_status check_table(const moe_expert_table &t, const char *name) {
-    if (!t.packed || !t.scales || !t.scale2)
+moe_status check_table(const moe_expert_table &t, const char *name, bool has_scales) {
+    if (!t.packed || (has_scales && !t.scales) || !t.scale2)
         return fail(MOE_ERR_INVALID_ARG, "%s expert table: NULL array", name);
-    if (!aligned(t.packed, 8) || !aligned(t.scales, 8) || !aligned(t.scale2, 4))
+    if (!aligned(t.packed, 8) || (has_scales && !aligned(t.scales, 8)) || !aligned(t.scale2, 4))
         return fail(MOE_ERR_INVALID_ARG, "%s expert table: misaligned array", name);
     return MOE_OK;
 }
@@ -196,13 +206,14 @@ moe_status check_weights(const moe_config *c, const moe_weights *w, bool experts
         (!w->shared_expert_gate || !aligned(w->shared_expert_gate, 16)))
         return fail(MOE_ERR_INVALID_ARG, "shared_gate=1 needs a 16-byte aligned shared_expert_gate");
     if (!experts) return MOE_OK;
-    if ((s = check_table(w->gate, "gate")) != MOE_OK) return s;
-    if ((s = check_table(w->up, "up")) != MOE_OK) return s;
-    if ((s = check_table(w->down, "down")) != MOE_OK) return s;
+    const bool sc = c->expert_fmt == MOE_EXPERT_NVFP4;
+    if ((s = check_table(w->gate, "gate", sc)) != MOE_OK) return s;
+    if ((s = check_table(w->up, "up", sc)) != MOE_OK) return s;
+    if ((s = check_table(w->down, "down", sc)) != MOE_OK) return s;
     if (c->has_shared) {
-        if ((s = check_mat(w->shared_gate_proj, "shared_gate_proj")) != MOE_OK) return s;
-        if ((s = check_mat(w->shared_up_proj, "shared_up_proj")) != MOE_OK) return s;
-        if ((s = check_mat(w->shared_down_proj, "shared_down_proj")) != MOE_OK) return s;
+        if ((s = check_mat(w->shared_gate_proj, "shared_gate_proj", sc)) != MOE_OK) return s;
+        if ((s = check_mat(w->shared_up_proj, "shared_up_proj", sc)) != MOE_OK) return s;
+        if ((s = check_mat(w->shared_down_proj, "shared_down_proj", sc)) != MOE_OK) return s;
     }
     return MOE_OK;
 }
@@ -401,8 +412,14 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     // transposed down matrix (16 x H/2 + H bytes: the size of a gate tile),
     // and there are no down units.
     const bool tl = cfg->t_layout != 0;
-    const size_t gu_slot = (size_t)kTileRows * (cfg->hidden / 2 + cfg->hidden / 16);
-    const size_t d_slot = tl ? 0 : (size_t)lp.down_rows * (L.inter_max / 2 + L.inter_max / 16);
+    // bytes of one row of K inputs in the expert format, block scales included
+    auto row_bytes = [cfg](int K) -> size_t {
+        return cfg->expert_fmt == MOE_EXPERT_FP8 ? (size_t)K
+               : cfg->expert_fmt == MOE_EXPERT_BF16 ? 2 * (size_t)K
+                                                    : (size_t)K / 2 + (size_t)K / 16;
+    };
+    const size_t gu_slot = (size_t)kTileRows * row_bytes(cfg->hidden);
+    const size_t d_slot = tl ? 0 : (size_t)lp.down_rows * row_bytes(L.inter_max);
     lp.slot_bytes = (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot);
     const int budget = di->smem_optin - 1024;
     int S = 16;
@@ -434,7 +451,8 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
         // gemv_lever applies per sub-chunk, so that a one-row last sub-chunk
         // gives the bytes of a one-row call
         e = launch_layer(lp, di->sms, layer_smem_bytes(S, lp.slot_bytes), mc_gu, tl ? 1 : mc_d,
-                         n == 1 && cfg->gemv_lever, tl, st);
+                         n == 1 && cfg->gemv_lever && cfg->expert_fmt == MOE_EXPERT_NVFP4, tl,
+                         cfg->expert_fmt, st);
     }
     if (e == cudaSuccess && nchunks > 1)
         e = launch_union(union_params(cfg, w, lp.ws.ids, rows, lp.ws, nullptr), st);

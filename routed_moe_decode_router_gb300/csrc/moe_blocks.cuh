@@ -13,11 +13,14 @@ namespace moe {
 // ---------------------------------------------------------------------------
 
 // Pointer entry (gate, up, down matrices) of expert x from the expert tables.
-__device__ __forceinline__ void load_ptr_entry(const moe_expert_table *tabs, int x, PtrEntry &e) {
+// (has_scales = 0: FP8 and BF16 experts, whose tables may hold no scale
+// arrays; the entry's scale pointers are then NULL and never read.)
+__device__ __forceinline__ void load_ptr_entry(const moe_expert_table *tabs, int x, PtrEntry &e,
+                                               bool has_scales) {
 #pragma unroll
     for (int m = 0; m < 3; ++m) {
         e.packed[m] = ld_cg(tabs[m].packed + x);
-        e.scales[m] = ld_cg(tabs[m].scales + x);
+        e.scales[m] = has_scales ? ld_cg(tabs[m].scales + x) : nullptr;
         e.scale2[m] = ld_cg(tabs[m].scale2 + x);
     }
     e.expert = x;
@@ -206,7 +209,7 @@ __device__ __forceinline__ void warp_topk_row(const float *lg, const float *bias
 // ---------------------------------------------------------------------------
 
 struct UnionSrc {
-    int E, k, rows, per_row_mode, has_tables, has_shared;
+    int E, k, rows, per_row_mode, has_tables, has_shared, has_scales;
     moe_expert_table gate, up, down;
     moe_nvfp4 sh_gate, sh_up, sh_down;
 };
@@ -235,8 +238,8 @@ __device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, ui
     PtrEntry pe[2];
     if (src.has_tables) {
         const moe_expert_table tb[3] = {src.gate, src.up, src.down};
-        load_ptr_entry(tb, min(max(id0, 0), src.E - 1), pe[0]);
-        if (n > 32) load_ptr_entry(tb, min(max(id1, 0), src.E - 1), pe[1]);
+        load_ptr_entry(tb, min(max(id0, 0), src.E - 1), pe[0], src.has_scales);
+        if (n > 32) load_ptr_entry(tb, min(max(id1, 0), src.E - 1), pe[1], src.has_scales);
     }
     const unsigned below = (1u << lane) - 1u;
     unsigned eq0, eq1, cross = 0;   // same-id lanes: half 0 for id0, half 1 for id1, half 0 for id1
@@ -375,6 +378,81 @@ __device__ __forceinline__ void chunk_mma(const uint8_t *pk, const uint8_t *sc, 
     }
 }
 
+// chunk_mma for FP8 expert tiles (one E4M3 code per weight, row_bytes = K,
+// no block scales): lane (g, q) reads the 32 codes of rows g and g+8 at
+// input offset q*32 of the chunk (two 16-byte loads a row); inputs 8t .. 8t+7
+// are bytes 8t .. 8t+7, converted pairwise (exact) into the same f16x2 order
+// that e2m1x8_to_f16x2 gives, so the MMA steps and B fragments are those of
+// chunk_mma.
+__device__ __forceinline__ void chunk_mma_fp8(const uint8_t *pk, int row_bytes, int c, int g,
+                                              int q, const uint32_t (&b)[8][2], float (&d0)[4],
+                                              float (&d1)[4]) {
+    const uint4 *ra = reinterpret_cast<const uint4 *>(pk + g * row_bytes + c * 128 + q * 32);
+    const uint4 *rb = reinterpret_cast<const uint4 *>(pk + (g + 8) * row_bytes + c * 128 + q * 32);
+    const uint4 a01[2] = {ra[0], ra[1]};
+    const uint4 b01[2] = {rb[0], rb[1]};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const uint4 &ua = a01[t >> 1], &ub = b01[t >> 1];
+        const uint32_t wa0 = (t & 1) ? ua.z : ua.x, wa1 = (t & 1) ? ua.w : ua.y;
+        const uint32_t wb0 = (t & 1) ? ub.z : ub.x, wb1 = (t & 1) ? ub.w : ub.y;
+        const uint32_t ha[4] = {e4m3x2_to_f16x2(wa0 & 0xFFFFu), e4m3x2_to_f16x2(wa0 >> 16),
+                                e4m3x2_to_f16x2(wa1 & 0xFFFFu), e4m3x2_to_f16x2(wa1 >> 16)};
+        const uint32_t hb[4] = {e4m3x2_to_f16x2(wb0 & 0xFFFFu), e4m3x2_to_f16x2(wb0 >> 16),
+                                e4m3x2_to_f16x2(wb1 & 0xFFFFu), e4m3x2_to_f16x2(wb1 >> 16)};
+        mma_f16_16816(d0, ha[0], hb[0], ha[1], hb[1], b[2 * t][0], b[2 * t][1]);
+        mma_f16_16816(d1, ha[2], hb[2], ha[3], hb[3], b[2 * t + 1][0], b[2 * t + 1][1]);
+    }
+}
+
+// chunk_mma for BF16 expert tiles (row_bytes = 2K): lane (g, q) reads the 32
+// bf16 weights of rows g and g+8 at input offset q*32 (four 16-byte loads a
+// row), which are already the A fragments of bf16 x bf16 MMAs; the B
+// fragments hold the token rows as raw bf16 (load_b with RAW).
+__device__ __forceinline__ void chunk_mma_bf16(const uint8_t *pk, int row_bytes, int c, int g,
+                                               int q, const uint32_t (&b)[8][2], float (&d0)[4],
+                                               float (&d1)[4]) {
+    const uint4 *ra = reinterpret_cast<const uint4 *>(pk + g * row_bytes + c * 256 + q * 64);
+    const uint4 *rb = reinterpret_cast<const uint4 *>(pk + (g + 8) * row_bytes + c * 256 + q * 64);
+    uint4 wa[4], wb[4];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        wa[t] = ra[t];
+        wb[t] = rb[t];
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        mma_bf16_16816(d0, wa[t].x, wb[t].x, wa[t].y, wb[t].y, b[2 * t][0], b[2 * t][1]);
+        mma_bf16_16816(d1, wa[t].z, wb[t].z, wa[t].w, wb[t].w, b[2 * t + 1][0], b[2 * t + 1][1]);
+    }
+}
+
+// Expert formats: 0 NVFP4, 1 FP8 (E4M3 per weight), 2 BF16.  Bytes of one
+// tile row of K inputs, and of its block scales.
+template <int FMT>
+__host__ __device__ constexpr uint32_t fmt_row_bytes(uint32_t K) {
+    return FMT == 0 ? K / 2 : (FMT == 1 ? K : 2 * K);
+}
+template <int FMT>
+__host__ __device__ constexpr uint32_t fmt_scale_row_bytes(uint32_t K) {
+    return FMT == 0 ? K / 16 : 0;
+}
+
+// One 128-input chunk of a 16-row tile in the expert format FMT (the scale
+// arguments are unused by FP8 and BF16).
+template <int FMT>
+__device__ __forceinline__ void chunk_mma_t(const uint8_t *pk, const uint8_t *sc, int row_bytes,
+                                            int sc_row_bytes, int c, int g, int q,
+                                            const uint32_t (&b)[8][2], float (&d0)[4],
+                                            float (&d1)[4]) {
+    if constexpr (FMT == 0)
+        chunk_mma(pk, sc, row_bytes, sc_row_bytes, c, g, q, b, d0, d1);
+    else if constexpr (FMT == 1)
+        chunk_mma_fp8(pk, row_bytes, c, g, q, b, d0, d1);
+    else
+        chunk_mma_bf16(pk, row_bytes, c, g, q, b, d0, d1);
+}
+
 // The one-row CUDA-core variant of chunk_mma (one token row, column 0): the
 // same lane data (rows g and g+8, inputs q*32..+31 of the chunk, their two
 // block scales) and the same B fragments, whose every lane holds token row
@@ -437,7 +515,9 @@ __device__ __forceinline__ void chunk_gemv(const uint8_t *pk, const uint8_t *sc,
 //
 // With ROW0 (the one-row CUDA-core variant) every lane takes token row 0, its
 // largest magnitude goes to [2^8, 2^9) instead, and inv0 = inv1 = 2^-e.
-template <int MAXC, bool ROW0 = false>
+// With RAW (BF16 expert tiles) the bf16 values stay as they are and
+// inv0 = inv1 = 1.
+template <int MAXC, bool ROW0 = false, bool RAW = false>
 __device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_stride,
                                        uint32_t mask, int nchunk, int warp, int nwarps,
                                        int lane, uint32_t (&b)[MAXC][8][2], float &inv0,
@@ -468,6 +548,10 @@ __device__ __forceinline__ void load_b(const uint16_t *rows_base, size_t row_str
             b[m][s2][0] = live ? b[m][s2][0] : 0u;
             b[m][s2][1] = live ? b[m][s2][1] : 0u;
         }
+    }
+    if constexpr (RAW) {
+        inv0 = inv1 = 1.f;
+        return;
     }
     float mx = 0.f;
 #pragma unroll

@@ -157,9 +157,12 @@ __device__ __forceinline__ void router_decode(const LayerParams &p, int row, uin
 // 2: <= 512, 3: <= 1024), so each instantiation holds one top-k variant;
 // GV: the one-row CUDA-core GEMV variant of the expert projections
 // (chunk_gemv) instead of the tensor-core MMA (chunk_mma); TL: the fused
-// one-row form for down projections in the t layout (MC_D unused).
-template <int MC_GU, int MC_D, int TK, bool GV, bool TL>
+// one-row form for down projections in the t layout (MC_D unused); FMT: the
+// expert format (0 NVFP4, 1 FP8, 2 BF16; the GEMV variant and the t layout
+// exist for NVFP4 only).
+template <int MC_GU, int MC_D, int TK, bool GV, bool TL, int FMT = 0>
 __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const LayerParams p) {
+    static_assert(FMT == 0 || (!GV && !TL), "GEMV variant and t layout: NVFP4 experts only");
     extern __shared__ __align__(128) uint8_t smem[];
     LayerSmem &sm = *reinterpret_cast<LayerSmem *>(smem);
     uint8_t *ring = smem + kLayerSmemFixed;
@@ -189,7 +192,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     const bool is_prod = warp == kProdWarp;
     const bool gate_row = p.has_shared && p.shared_gated;
     const int nrow = E + (gate_row ? 1 : 0);
-    const uint32_t gu_pk = kTileRows * H / 2, gu_sc = kTileRows * H / 16;
+    const uint32_t gu_pk = kTileRows * fmt_row_bytes<FMT>(H);
+    const uint32_t gu_sc = kTileRows * fmt_scale_row_bytes<FMT>(H);
     WsHeader *hdr = p.ws.hdr;
 
     if (tid == 0) {
@@ -223,7 +227,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         uint8_t *st = ring + (size_t)s * p.slot_bytes;
         mbar_arrive_expect_tx(&full[s], pkb + scb);
         bulk_g2s(st, pk, pkb, &full[s], pol);
-        bulk_g2s(st + pkb, sc, scb, &full[s], pol);
+        if (scb) bulk_g2s(st + pkb, sc, scb, &full[s], pol);   // FP8 / BF16: no block scales
         ++pi;
     };
     auto issue_empty = [&]() -> bool {
@@ -416,8 +420,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     __syncthreads();
     if (warp == kEpiWarp) {
         MOE_TIC(t_union);
-        UnionSrc src{E,      k,      p.rows, p.per_row_mode, 1,        p.has_shared,
-                     p.gate, p.up,   p.down, p.sh_gate,      p.sh_up, p.sh_down};
+        UnionSrc src{E,      k,      p.rows,  p.per_row_mode, 1,       p.has_shared, FMT == 0,
+                     p.gate, p.up,   p.down,  p.sh_gate,      p.sh_up, p.sh_down};
         build_union(src, sm.ids, sm.umask, &sm.uni, sm.ptrs, hdr, lane);
         __syncwarp();
         asm volatile("bar.arrive 4, %0;" ::"r"(kLayerThreads) : "memory");
@@ -477,8 +481,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 int K;
                 if (j < Sd) {
                     K = p.Is;
-                    dp = p.sh_down.packed + (size_t)j * DR * (K / 2);
-                    ds = p.sh_down.scales + (size_t)j * DR * (K / 16);
+                    dp = p.sh_down.packed + (size_t)j * DR * fmt_row_bytes<FMT>(K);
+                    ds = p.sh_down.scales + (size_t)j * DR * fmt_scale_row_bytes<FMT>(K);
                 } else {
                     const PtrEntry &e = sm.ptrs[(j - Sd) / Hd];
                     const int tile = (j - Sd) % Hd;
@@ -487,11 +491,11 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         continue;
                     }
                     K = p.I;
-                    dp = e.packed[2] + (size_t)tile * DR * (K / 2);
-                    ds = e.scales[2] + (size_t)tile * DR * (K / 16);
+                    dp = e.packed[2] + (size_t)tile * DR * fmt_row_bytes<FMT>(K);
+                    ds = e.scales[2] + (size_t)tile * DR * fmt_scale_row_bytes<FMT>(K);
                 }
                 if (!(ok = acquire(pi))) break;
-                issue_pair(dp, ds, DR * K / 2, DR * K / 16);
+                issue_pair(dp, ds, DR * fmt_row_bytes<FMT>(K), DR * fmt_scale_row_bytes<FMT>(K));
             }
             MOE_PHASE_MARK(true, 10);
         }
@@ -854,8 +858,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         {
             uint32_t bx[MC_GU][8][2];
             float inv0, inv1;
-            load_b<MC_GU, GV>(p.x, (size_t)H, allrows, H / kChunk, warp, kConsumerWarps, lane,
-                              bx, inv0, inv1);
+            load_b<MC_GU, GV, FMT == 2>(p.x, (size_t)H, allrows, H / kChunk, warp,
+                                        kConsumerWarps, lane, bx, inv0, inv1);
             MOE_PHASE_MARK(tid == 0, 5);
             named_bar(4, kLayerThreads);
             sweep_layout();
@@ -897,8 +901,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                                 du0[0] += ua;
                                 du0[2] += ub;
                             } else {
-                                chunk_mma(sg, sg + gu_pk, H / 2, H / 16, c, g, q, bx[m], dg0, dg1);
-                                chunk_mma(su, su + gu_pk, H / 2, H / 16, c, g, q, bx[m], du0, du1);
+                                chunk_mma_t<FMT>(sg, sg + gu_pk, fmt_row_bytes<FMT>(H),
+                                                 fmt_scale_row_bytes<FMT>(H), c, g, q, bx[m], dg0, dg1);
+                                chunk_mma_t<FMT>(su, su + gu_pk, fmt_row_bytes<FMT>(H),
+                                                 fmt_scale_row_bytes<FMT>(H), c, g, q, bx[m], du0, du1);
                             }
                         }
                     }
@@ -1002,14 +1008,14 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     jend = min(Sd + (entry + 1) * Hd, d_end);
                 }
                 const int nch = K / kChunk;
-                const uint32_t rowb = (uint32_t)K / 2, scb = (uint32_t)K / 16;
+                const uint32_t rowb = fmt_row_bytes<FMT>(K), scb = fmt_scale_row_bytes<FMT>(K);
                 // wide units: this warp's chunk and tile group
                 // (split units: chunk group warp % 4, tile warp / 4)
                 const int cw = wide ? warp % nch : (split ? warp % 4 : warp);
                 const int gw = wide ? warp / nch : (split ? warp / 4 : 0);
                 const int tpg = nch / 2;
                 MOE_TIC(t_b);
-                load_b<MC_D, GV>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
+                load_b<MC_D, GV, FMT == 2>(p.ws.hbuf + (size_t)entry * kMaxRows * p.ws.inter_max,
                              (size_t)p.ws.inter_max, mask, nch, cw,
                              wide ? nch : (split ? 4 : kConsumerWarps), lane, bh, inv0, inv1);
                 MOE_TOC(tid == 0, 21, t_b);
@@ -1040,9 +1046,9 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                                 c0[0] = yc;
                                 c0[2] = yd;
                             } else {
-                                chunk_mma(st + t0 * kTileRows * rowb, sc + t0 * kTileRows * scb, rowb,
+                                chunk_mma_t<FMT>(st + t0 * kTileRows * rowb, sc + t0 * kTileRows * scb, rowb,
                                           scb, cw, g, q, bh[0], a0, a1);
-                                chunk_mma(st + t1 * kTileRows * rowb, sc + t1 * kTileRows * scb, rowb,
+                                chunk_mma_t<FMT>(st + t1 * kTileRows * rowb, sc + t1 * kTileRows * scb, rowb,
                                           scb, cw, g, q, bh[0], c0, c1);
                             }
                         }
@@ -1060,7 +1066,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                                         a0[0] += ya;
                                         a0[2] += yb;
                                     } else {
-                                        chunk_mma(st + gw * kTileRows * rowb, sc + gw * kTileRows * scb,
+                                        chunk_mma_t<FMT>(st + gw * kTileRows * rowb, sc + gw * kTileRows * scb,
                                                   rowb, scb, c, g, q, bh[m], a0, a1);
                                     }
                                 }
@@ -1081,8 +1087,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                                     c0[0] += yc;
                                     c0[2] += yd;
                                 } else {
-                                    chunk_mma(st, sc, rowb, scb, c, g, q, bh[m], a0, a1);
-                                    chunk_mma(st + kTileRows * rowb, sc + kTileRows * scb, rowb,
+                                    chunk_mma_t<FMT>(st, sc, rowb, scb, c, g, q, bh[m], a0, a1);
+                                    chunk_mma_t<FMT>(st + kTileRows * rowb, sc + kTileRows * scb, rowb,
                                               scb, c, g, q, bh[m], c0, c1);
                                 }
                             }
@@ -1139,18 +1145,19 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     MOE_PHASE_MARK(tid == 0, 9);
 }
 
-// The sixteen (MC_GU, MC_D) instantiations of one top-k class and variant.
-template <int TK, bool GV>
+// The sixteen (MC_GU, MC_D) instantiations of one top-k class, projection
+// variant and expert format.
+template <int TK, bool GV, int FMT = 0>
 void *layer_kernel_table(int mc_gu, int mc_d) {
     static void *const tab[4][4] = {
-        {(void *)moe_layer_kernel<1, 1, TK, GV, false>, (void *)moe_layer_kernel<1, 2, TK, GV, false>,
-         (void *)moe_layer_kernel<1, 3, TK, GV, false>, (void *)moe_layer_kernel<1, 4, TK, GV, false>},
-        {(void *)moe_layer_kernel<2, 1, TK, GV, false>, (void *)moe_layer_kernel<2, 2, TK, GV, false>,
-         (void *)moe_layer_kernel<2, 3, TK, GV, false>, (void *)moe_layer_kernel<2, 4, TK, GV, false>},
-        {(void *)moe_layer_kernel<3, 1, TK, GV, false>, (void *)moe_layer_kernel<3, 2, TK, GV, false>,
-         (void *)moe_layer_kernel<3, 3, TK, GV, false>, (void *)moe_layer_kernel<3, 4, TK, GV, false>},
-        {(void *)moe_layer_kernel<4, 1, TK, GV, false>, (void *)moe_layer_kernel<4, 2, TK, GV, false>,
-         (void *)moe_layer_kernel<4, 3, TK, GV, false>, (void *)moe_layer_kernel<4, 4, TK, GV, false>}};
+        {(void *)moe_layer_kernel<1, 1, TK, GV, false, FMT>, (void *)moe_layer_kernel<1, 2, TK, GV, false, FMT>,
+         (void *)moe_layer_kernel<1, 3, TK, GV, false, FMT>, (void *)moe_layer_kernel<1, 4, TK, GV, false, FMT>},
+        {(void *)moe_layer_kernel<2, 1, TK, GV, false, FMT>, (void *)moe_layer_kernel<2, 2, TK, GV, false, FMT>,
+         (void *)moe_layer_kernel<2, 3, TK, GV, false, FMT>, (void *)moe_layer_kernel<2, 4, TK, GV, false, FMT>},
+        {(void *)moe_layer_kernel<3, 1, TK, GV, false, FMT>, (void *)moe_layer_kernel<3, 2, TK, GV, false, FMT>,
+         (void *)moe_layer_kernel<3, 3, TK, GV, false, FMT>, (void *)moe_layer_kernel<3, 4, TK, GV, false, FMT>},
+        {(void *)moe_layer_kernel<4, 1, TK, GV, false, FMT>, (void *)moe_layer_kernel<4, 2, TK, GV, false, FMT>,
+         (void *)moe_layer_kernel<4, 3, TK, GV, false, FMT>, (void *)moe_layer_kernel<4, 4, TK, GV, false, FMT>}};
     if (mc_gu < 1 || mc_gu > 4 || mc_d < 1 || mc_d > 4) return nullptr;
     return tab[mc_gu - 1][mc_d - 1];
 }

@@ -161,7 +161,7 @@ struct RouteParams {
 // Parameters of the union kernel (moe_union, and calls of several
 // sub-chunks): up to kCallIds ids.
 struct UnionParams {
-    int E, k, rows, per_row_mode, has_tables, has_shared;
+    int E, k, rows, per_row_mode, has_tables, has_shared, has_scales;
     const int32_t *ids;
     moe_expert_table gate, up, down;
     moe_nvfp4 sh_gate, sh_up, sh_down;

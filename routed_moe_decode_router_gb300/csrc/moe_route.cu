@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kCallIds) moe_union_kernel(const UnionParams p
                 e.expert = -1;
             } else {
                 const moe_expert_table tb[3] = {p.gate, p.up, p.down};
-                load_ptr_entry(tb, id, e);
+                load_ptr_entry(tb, id, e, p.has_scales != 0);
                 bool ok = true;
 #pragma unroll
                 for (int m = 0; m < 3; ++m) ok = ok && aligned16(e.packed[m]) && aligned16(e.scales[m]);

@@ -25,7 +25,9 @@ def make_config(shape: MoeShape, per_row_mode: bool = False, gemv: bool = False,
         routed_scaling_factor=float(shape.routed_scaling_factor),
         router_fmt=N.MOE_ROUTER_NVFP4 if shape.router_fmt == "nvfp4" else N.MOE_ROUTER_BF16,
         has_shared=int(shape.has_shared), shared_gate=int(shape.shared_gated),
-        per_row_mode=int(per_row_mode), gemv_lever=int(gemv), t_layout=int(t_layout))
+        per_row_mode=int(per_row_mode), gemv_lever=int(gemv), t_layout=int(t_layout),
+        expert_fmt={"nvfp4": N.MOE_EXPERT_NVFP4, "fp8": N.MOE_EXPERT_FP8,
+                    "bf16": N.MOE_EXPERT_BF16}[shape.expert_fmt])
 
 
 def _ptr(t: Optional[torch.Tensor]) -> int:
@@ -89,6 +91,8 @@ class DeviceLayer:
         down = layer.down
         sh_down = layer.sh_down if s.has_shared else None
         if self.t_layout:
+            if s.expert_fmt != "nvfp4":
+                raise ValueError("the t layout holds NVFP4 down projections only")
             stream = _stream(None)
             down = self._to_t(down, E, s.hidden, s.moe_inter, stream)
             if s.has_shared:
@@ -111,19 +115,21 @@ class DeviceLayer:
             sc = m.scales.reshape(E, -1)
             pk_ptrs = (pk.data_ptr() + torch.arange(E, dtype=torch.int64) *
                        pk.stride(0)).to(device)
+            # FP8 / BF16 experts have no block scales: NULL scale arrays
             sc_ptrs = (sc.data_ptr() + torch.arange(E, dtype=torch.int64) *
-                       sc.stride(0)).to(device)
+                       sc.stride(0)).to(device) if s.expert_fmt == "nvfp4" else None
             s2 = m.scale2.float().contiguous()
             self._tables[name] = (pk_ptrs, sc_ptrs, s2)
-            setattr(w, name, N.ExpertTable(pk_ptrs.data_ptr(), sc_ptrs.data_ptr(),
+            setattr(w, name, N.ExpertTable(pk_ptrs.data_ptr(), _ptr(sc_ptrs),
                                            s2.data_ptr()))
         if s.has_shared:
             for name, field in (("sh_gate", "shared_gate_proj"),
                                 ("sh_up", "shared_up_proj"),
                                 ("sh_down", "shared_down_proj")):
                 m = sh_down if name == "sh_down" else getattr(layer, name)
-                setattr(w, field, N.Nvfp4Desc(m.packed.data_ptr(), m.scales.data_ptr(),
-                                              float(m.scale2)))
+                setattr(w, field, N.Nvfp4Desc(
+                    m.packed.data_ptr(), m.scales.data_ptr() if s.expert_fmt == "nvfp4" else 0,
+                    float(m.scale2)))
             if s.shared_gated:
                 w.shared_expert_gate = layer.sh_gate_vec.data_ptr()
         self.weights = w

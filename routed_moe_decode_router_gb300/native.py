@@ -20,6 +20,7 @@ MOE_CHUNK_IDS = 64
 MOE_STATIC_WORKSPACE_BYTES = 10 << 20
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 MOE_ROUTER_BF16, MOE_ROUTER_NVFP4 = 0, 1
+MOE_EXPERT_NVFP4, MOE_EXPERT_FP8, MOE_EXPERT_BF16 = 0, 1, 2
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_STATUS"}
@@ -46,7 +47,7 @@ class MoeConfig(C.Structure):
                 ("routed_scaling_factor", C.c_float), ("router_fmt", C.c_int),
                 ("has_shared", C.c_int), ("shared_gate", C.c_int),
                 ("per_row_mode", C.c_int), ("gemv_lever", C.c_int),
-                ("t_layout", C.c_int)]
+                ("t_layout", C.c_int), ("expert_fmt", C.c_int)]
 
 
 class ExpertTable(C.Structure):

@@ -91,6 +91,8 @@ def good_cfg(**kw):
     ("per_row_mode", 2, N.MoeError),
     ("gemv_lever", 2, N.MoeError),
     ("t_layout", 2, N.MoeError),
+    ("expert_fmt", 3, N.MoeError),
+    ("expert_fmt", -1, N.MoeError),
 ])
 def test_config_refusals(lib, field, value, status):
     cfg = good_cfg(**{field: value})
@@ -131,6 +133,30 @@ def test_t_layout_workspace_holds_one_partial_row_per_cta(lib):
         a = N.moe_workspace_size(L.make_config(wl.shape))
         b = N.moe_workspace_size(L.make_config(wl.shape, t_layout=True))
         assert b - a == 256 * wl.shape.hidden * 4, name
+
+
+def test_t_layout_needs_nvfp4_experts(lib):
+    for fmt in (N.MOE_EXPERT_FP8, N.MOE_EXPERT_BF16):
+        N.moe_check_config(good_cfg(expert_fmt=fmt))
+        with pytest.raises(N.MoeError) as ei:
+            N.moe_check_config(good_cfg(expert_fmt=fmt, t_layout=1))
+        assert ei.value.status == 2
+
+
+def test_fp8_and_bf16_expert_tables_need_no_scales(lib):
+    """FP8 / BF16 experts: NULL scale arrays pass the host checks (the call
+    then stops at the NULL workspace); NVFP4 experts refuse them."""
+    shape = synth.WORKLOADS["tiny_h256_e16"].shape
+    for fmt, ok in ((N.MOE_EXPERT_NVFP4, False), (N.MOE_EXPERT_FP8, True),
+                    (N.MOE_EXPERT_BF16, True)):
+        cfg = good_cfg(expert_fmt=fmt)
+        w = fake_weights()
+        w.gate = w.up = w.down = N.ExpertTable(FAKE, 0, FAKE)
+        d = N.Nvfp4Desc(FAKE, 0, 1.0)
+        w.shared_gate_proj = w.shared_up_proj = w.shared_down_proj = d
+        with pytest.raises(N.MoeError) as ei:
+            N.moe_forward(cfg, w, FAKE, FAKE + (1 << 20), 1, 0, 1 << 20, 0)
+        assert ("workspace" in str(ei.value)) == ok, (fmt, str(ei.value))
 
 
 def test_largest_config_fits_the_static_workspace(lib):

@@ -91,6 +91,20 @@ def test_layer_bytes_other_workloads(workload, rows, U, want_mb):
     assert abs(mb - want_mb) < 0.15, (mb, want_mb)
 
 
+@pytest.mark.parametrize("fmt,per_weight", [("fp8", 1), ("bf16", 2)])
+def test_layer_bytes_other_expert_formats(fmt, per_weight):
+    """FP8 / BF16 experts: 1 / 2 bytes per weight and no block scales; the
+    router and the rest are unchanged."""
+    import dataclasses
+
+    import bench
+    from routed_moe_decode_router_gb300 import synth
+    shape = dataclasses.replace(synth.WORKLOADS["decode_h2048_e128"].shape, expert_fmt=fmt)
+    per_expert = 3 * 2048 * 768 * per_weight + 12
+    want = 9 * per_expert + 128 * 2048 * 9 // 16 + 4 + 2048 * 2 + 2 * 2048 * 2
+    assert bench.layer_bytes(shape, 1, 8) == want
+
+
 def test_layer_bytes_variant_terms():
     """Each optional term enters exactly once: no shared expert, an ungated
     shared expert (no gate vector), an NVFP4 router (9/16 byte per weight +
@@ -165,6 +179,7 @@ def test_committed_traffic_keyed_to_kernel_workload_rows_and_sources(tmp_path, m
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc123")
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1) == 24182016
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1, True) == 24100000
+    assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1, False, "fp8") is None
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 8) is None
     assert bench.committed_traffic("moe_layer_kernel", "prefill8_h2048_e512", 1) is None
     assert bench.committed_traffic("moe_route_kernel", "decode_h2048_e128", 1) is None
