@@ -226,12 +226,14 @@ class ClockSampler:
 # Workload
 # ---------------------------------------------------------------------------
 
-def build_workload(name, rows, n_layers, device, t_layout=False):
+def build_workload(name, rows, n_layers, device, t_layout=False, fmt="nvfp4"):
+    import dataclasses
+
     import torch
     from routed_moe_decode_router_gb300 import layer as L
     from routed_moe_decode_router_gb300 import synth
     wl = synth.WORKLOADS[name]
-    shape = wl.shape
+    shape = dataclasses.replace(wl.shape, expert_fmt=fmt)
     layers = [L.DeviceLayer(synth.make_layer(shape, wl.seed_base + l, device=device),
                             device=device, t_layout=t_layout) for l in range(n_layers)]
     xbuf = torch.empty((n_layers, rows, shape.hidden), dtype=torch.bfloat16, device=device)
@@ -399,6 +401,15 @@ EXTRA_CONFIGS = [
 ]
 
 
+def launches_per_layer(shape, rows: int, t_layout: bool) -> int:
+    """Kernel launches of one moe_forward: one per sub-chunk (min(8, 64/k)
+    rows; one row with the t layout), plus the union kernel when a call has
+    more than one sub-chunk."""
+    cr = 1 if t_layout else min(8, 64 // shape.top_k)
+    n = (rows + cr - 1) // cr
+    return n + (1 if n > 1 else 0)
+
+
 def use_t_layout(choice: str, rows: int) -> bool:
     return choice == "t" or (choice == "auto" and rows == 1)
 
@@ -463,8 +474,9 @@ def run_ours(args, rank, world, local):
     wl0 = synth.WORKLOADS[args.workload]
     rows = args.rows or max(wl0.rows)
     n_layers = args.layers or wl0.layers
-    t_layout = use_t_layout(args.down_layout, rows)
-    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev, t_layout)
+    t_layout = use_t_layout(args.down_layout, rows) and args.expert_fmt == "nvfp4"
+    wl, shape, layers, xbuf, outbuf = build_workload(args.workload, rows, n_layers, dev, t_layout,
+                                                     args.expert_fmt)
     from routed_moe_decode_router_gb300 import layer as L
     ws = L.Workspace(shape, device=dev, t_layout=t_layout)
     stream = torch.cuda.Stream(device=dev)
@@ -485,7 +497,8 @@ def run_ours(args, rank, world, local):
     step_bytes = sum(layer_bytes(shape, rows, u) for u in U)
     peak, peak_kind = hbm_peak()
     achieved = step_bytes / n_layers / (kernel_ms * 1e-3) / 1e9
-    traffic = committed_traffic("moe_layer_kernel", args.workload, rows, t_layout)
+    traffic = committed_traffic("moe_layer_kernel", args.workload, rows, t_layout,
+                                args.expert_fmt)
 
     # end to end through the public API with host buffers
     x_host = xbuf.cpu().pin_memory()
@@ -504,6 +517,24 @@ def run_ours(args, rank, world, local):
     t1.synchronize()
     e2e_ms = max_over_ranks(t0.elapsed_time(t1))
     e2e_value = aggregate_us_per_unit(e2e_ms, e2e_steps * n_layers, world)
+    # the same end to end with one eager public-API call per layer (no
+    # graph): the host side of every call (binding, argument checks, launch)
+    # is inside the timed region too
+    eager_steps = max(1, min(args.steps, 50))
+    for l, dl in enumerate(layers):   # warm-up of the eager path
+        L.forward(dl, xbuf[l], ws, out=outbuf[l], gemv=args.gemv)
+    torch.cuda.synchronize()
+    barrier()
+    t0.record()
+    for _ in range(eager_steps):
+        xbuf.copy_(x_host, non_blocking=True)
+        for l, dl in enumerate(layers):
+            L.forward(dl, xbuf[l], ws, out=outbuf[l], gemv=args.gemv)
+        out_host.copy_(outbuf, non_blocking=True)
+    t1.record()
+    t1.synchronize()
+    eager_ms = max_over_ranks(t0.elapsed_time(t1))
+    eager_value = aggregate_us_per_unit(eager_ms, eager_steps * n_layers, world)
     if ws.status() != 0:
         raise RuntimeError("device status set during the timed region")
 
@@ -512,10 +543,13 @@ def run_ours(args, rank, world, local):
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16 mma / f32 accumulate (nvfp4 weights, bf16 activations)",
-        "data": "synthetic (seeded N(0,0.02) weights quantised to NVFP4, bf16 activations)",
+        "dtype": ("bf16" if args.expert_fmt == "bf16" else "f16")
+                 + " mma / f32 accumulate (%s weights, bf16 activations)" % args.expert_fmt,
+        "data": "synthetic (seeded N(0,0.02) weights encoded as %s, bf16 activations)"
+                % args.expert_fmt.upper(),
         "config": workload_config(wl, shape, rows, n_layers, {
             "gemv_lever": int(args.gemv and rows == 1),
+            "expert_fmt": args.expert_fmt,
             "down_layout": "t (input-major)" if t_layout else "output-major",
             "union_mean": round(sum(U) / len(U), 3),
             "l2": "no flush: each step streams %.2f GB of distinct weights (L2 129 MB)"
@@ -538,8 +572,11 @@ def run_ours(args, rank, world, local):
                              "dependent launch overlaps consecutive layers"},
         "e2e": {"value": round(e2e_value, 4), "unit": UNIT,
                 "h2d_bytes_per_step": int(x_host.numel() * 2),
-                "d2h_bytes_per_step": int(out_host.numel() * 2)},
-        "gpu_launches": n_layers * args.steps,
+                "d2h_bytes_per_step": int(out_host.numel() * 2),
+                "path": "graph replay of the public API calls",
+                "eager_value": round(eager_value, 4),
+                "eager_path": "one Python-level moe_forward per layer per step, no graph"},
+        "gpu_launches": n_layers * args.steps * launches_per_layer(shape, rows, t_layout),
         "clocks": clocks,
     }
     do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
@@ -628,6 +665,8 @@ def main(argv=None):
     ap.add_argument("--cpu-1core-s", type=float, default=5.0)
     ap.add_argument("--gemv", action="store_true",
                     help="one-row layers on the CUDA-core GEMV variant (gemv_lever = 1)")
+    ap.add_argument("--expert-fmt", choices=["nvfp4", "fp8", "bf16"], default="nvfp4",
+                    help="expert matrix format (the t layout is NVFP4 only)")
     ap.add_argument("--down-layout", choices=["auto", "t", "output"], default="auto",
                     help="down projections in the t layout (the fused one-row form) or "
                          "output-major; auto = t for one-row workloads")

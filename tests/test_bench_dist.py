@@ -252,3 +252,13 @@ def test_parity_verdict_bar():
     v = bench.parity_verdict([(torch.from_numpy(want).to(torch.bfloat16), want),
                               (torch.from_numpy(bad).to(torch.bfloat16), want)])
     assert not v["ok"] and v["max_abs"] > 3e-2
+
+
+def test_launches_per_layer():
+    import bench
+    from routed_moe_decode_router_gb300 import synth
+    dec = synth.WORKLOADS["decode_h2048_e128"].shape       # top_k 8: 8-row sub-chunks
+    assert bench.launches_per_layer(dec, 1, True) == 1
+    assert bench.launches_per_layer(dec, 8, False) == 1
+    assert bench.launches_per_layer(dec, 16, False) == 3  # two sub-chunks + the union kernel
+    assert bench.launches_per_layer(dec, 3, True) == 4    # one launch per row + the union
