@@ -113,9 +113,11 @@ enum { MOE_ROUTER_BF16 = 0, MOE_ROUTER_NVFP4 = 1 };
  * The forward_token_major.rs page names BF16 and FP8 experts as formats its
  * token-major path hands to another path, without giving their layout; the
  * layouts above are this library's reading.  A 16-row tile of an FP8 or
- * BF16 matrix is 16*K or 32*K bytes: configurations whose gate/up or down
- * tiles do not fit two shared-memory ring slots are refused at the first
- * forward (MOE_ERR_UNSUPPORTED; BF16 at hidden 4096, for example). */
+ * BF16 matrix is 16*K or 32*K bytes.  BF16 gate/up tiles too large for two
+ * shared-memory ring slots are streamed in two K-halves (hidden up to 4096,
+ * when hidden/128 is even); configurations whose tiles still do not fit
+ * (BF16 down tiles of intermediates of 2048 or more, for example) are
+ * refused at the first forward (MOE_ERR_UNSUPPORTED). */
 enum { MOE_EXPERT_NVFP4 = 0, MOE_EXPERT_FP8 = 1, MOE_EXPERT_BF16 = 2 };
 
 /* One NVFP4 matrix whose pointers the host knows (router, shared expert). */

@@ -418,10 +418,18 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
                : cfg->expert_fmt == MOE_EXPERT_BF16 ? 2 * (size_t)K
                                                     : (size_t)K / 2 + (size_t)K / 16;
     };
-    const size_t gu_slot = (size_t)kTileRows * row_bytes(cfg->hidden);
+    size_t gu_slot = (size_t)kTileRows * row_bytes(cfg->hidden);
     const size_t d_slot = tl ? 0 : (size_t)lp.down_rows * row_bytes(L.inter_max);
-    lp.slot_bytes = (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot);
     const int budget = di->smem_optin - 1024;
+    // BF16 gate/up tiles that do not fit two ring slots are taken in two
+    // K-halves (each half a whole number of 128-input chunks)
+    lp.gu_halves = 1;
+    if (cfg->expert_fmt == MOE_EXPERT_BF16 && layer_smem_bytes(2, (uint32_t)gu_slot) > (size_t)budget &&
+        (cfg->hidden / kChunk) % 2 == 0) {
+        lp.gu_halves = 2;
+        gu_slot /= 2;
+    }
+    lp.slot_bytes = (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot);
     int S = 16;
     while (S > 2 && layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget) --S;
     if (layer_smem_bytes(S, lp.slot_bytes) > (size_t)budget || (tl && S < 4))

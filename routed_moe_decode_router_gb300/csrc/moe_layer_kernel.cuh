@@ -230,6 +230,15 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         if (scb) bulk_g2s(st + pkb, sc, scb, &full[s], pol);   // FP8 / BF16: no block scales
         ++pi;
     };
+    // n rows of seg bytes at a source stride into one slot
+    auto issue_rows = [&](const uint8_t *src, uint32_t stride, uint32_t seg, int n) {
+        const int s = pi % S;
+        uint8_t *st = ring + (size_t)s * p.slot_bytes;
+        mbar_arrive_expect_tx(&full[s], seg * (uint32_t)n);
+        for (int r = 0; r < n; ++r)
+            bulk_g2s(st + (size_t)r * seg, src + (size_t)r * stride, seg, &full[s], pol);
+        ++pi;
+    };
     auto issue_empty = [&]() -> bool {
         if (!acquire(pi)) return false;
         mbar_arrive(&full[pi % S]);
@@ -239,7 +248,11 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     // gate+up unit j (16 rows): a gate slot, then an up slot; in the t
     // layout also a slot with the unit's 16 rows of the transposed down
     // matrix (16 x H/2 packed bytes, then the H scales of that block)
-    constexpr int kUnitSlots = TL ? 3 : 2;
+    // BF16 gate/up tiles too large for the ring come in two K-halves: a unit
+    // is then gate half 0, up half 0, gate half 1, up half 1 (a half tile is
+    // 16 row segments of H bytes, one bulk copy each)
+    const int ghalves = (FMT == 2) ? p.gu_halves : 1;
+    const int kUnitSlots = TL ? 3 : 2 * ghalves;
     const uint32_t dt_pk = kTileRows * H / 2, dt_sc = H;
     auto issue_gu = [&](int j) -> bool {
         const uint8_t *gp, *gs, *upk, *us, *dp = nullptr, *ds = nullptr;
@@ -255,8 +268,11 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         } else {
             const PtrEntry &e = sm.ptrs[(j - St) / It];
             const int tile = (j - St) % It;
-            if (e.expert < 0)
-                return issue_empty() && issue_empty() && (!TL || issue_empty());
+            if (e.expert < 0) {
+                bool ok2 = true;
+                for (int i = 0; i < kUnitSlots; ++i) ok2 = ok2 && issue_empty();
+                return ok2;
+            }
             gp = e.packed[0] + (size_t)tile * gu_pk;
             gs = e.scales[0] + (size_t)tile * gu_sc;
             upk = e.packed[1] + (size_t)tile * gu_pk;
@@ -265,6 +281,16 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 dp = e.packed[2] + (size_t)tile * dt_pk;
                 ds = e.scales[2] + (size_t)tile * dt_sc;
             }
+        }
+        if (FMT == 2 && ghalves == 2) {
+            const uint32_t row = fmt_row_bytes<FMT>(H), half = row / 2;
+            for (int h = 0; h < 2; ++h) {
+                if (!acquire(pi)) return false;
+                issue_rows(gp + h * half, row, half, kTileRows);
+                if (!acquire(pi)) return false;
+                issue_rows(upk + h * half, row, half, kTileRows);
+            }
+            return true;
         }
         if (!acquire(pi)) return false;
         issue_pair(gp, gs, gu_pk, gu_sc);
@@ -887,7 +913,54 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 const uint8_t *su = ring + (size_t)s1 * p.slot_bytes;
                 float dg0[4] = {0.f, 0.f, 0.f, 0.f}, dg1[4] = {0.f, 0.f, 0.f, 0.f};
                 float du0[4] = {0.f, 0.f, 0.f, 0.f}, du1[4] = {0.f, 0.f, 0.f, 0.f};
-                if (ok0 && ok1) {
+                if (FMT == 2 && ghalves == 2) {
+                    // K-halves (BF16): this warp's chunks below nh from the
+                    // first pair of slots, the rest from the second pair, in
+                    // the same chunk order as a whole tile
+                    const int nh = nch / 2;
+                    const uint32_t hrow = fmt_row_bytes<FMT>(H) / 2;
+                    if (ok0 && ok1) {
+#pragma unroll
+                        for (int m = 0; m < MC_GU; ++m) {
+                            const int c = warp + kConsumerWarps * m;
+                            if (c < nh) {
+                                chunk_mma_t<FMT>(sg, sg, hrow, 0, c, g, q, bx[m], dg0, dg1);
+                                chunk_mma_t<FMT>(su, su, hrow, 0, c, g, q, bx[m], du0, du1);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&empty[s0]);
+                        mbar_arrive(&empty[s1]);
+                    }
+                    const int s2h = rs;
+                    const uint32_t p2h = rp;
+                    next_slot();
+                    const int s3h = rs;
+                    const uint32_t p3h = rp;
+                    next_slot();
+                    const bool ok2 = ring_wait(&full[s2h], p2h, abort, hdr, (uint32_t)ci + 2);
+                    const bool ok3 = ring_wait(&full[s3h], p3h, abort, hdr, (uint32_t)ci + 3);
+                    const uint8_t *sg2 = ring + (size_t)s2h * p.slot_bytes;
+                    const uint8_t *su2 = ring + (size_t)s3h * p.slot_bytes;
+                    if (ok2 && ok3) {
+#pragma unroll
+                        for (int m = 0; m < MC_GU; ++m) {
+                            const int c = warp + kConsumerWarps * m;
+                            if (c >= nh && c < nch) {
+                                chunk_mma_t<FMT>(sg2, sg2, hrow, 0, c - nh, g, q, bx[m], dg0, dg1);
+                                chunk_mma_t<FMT>(su2, su2, hrow, 0, c - nh, g, q, bx[m], du0, du1);
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&empty[s2h]);
+                        mbar_arrive(&empty[s3h]);
+                    }
+                    ci += 2;
+                } else if (ok0 && ok1) {
 #pragma unroll
                     for (int m = 0; m < MC_GU; ++m) {
                         const int c = warp + kConsumerWarps * m;
@@ -909,10 +982,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         }
                     }
                 }
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&empty[s0]);
-                    mbar_arrive(&empty[s1]);
+                if (!(FMT == 2 && ghalves == 2)) {
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&empty[s0]);
+                        mbar_arrive(&empty[s1]);
+                    }
                 }
                 ci += 2;
                 float dg[4], du[4];

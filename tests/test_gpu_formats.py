@@ -1,8 +1,9 @@
 """FP8 and BF16 expert matrices on the GPU: oracle parity (the oracle decodes
 the same bytes in its own code), union mode byte-identical to per-row mode,
-calls of several sub-chunks, degenerate routings, the full-size shapes that
-fit, the refusal of BF16 tiles that do not fit the shared-memory ring, and
-CUDA-graph replay."""
+calls of several sub-chunks, degenerate routings, BF16 gate/up tiles taken in
+two K-halves (hidden 3584 and 4096), the full-size shapes, the refusal of
+BF16 down tiles that do not fit the shared-memory ring, and CUDA-graph
+replay."""
 import pytest
 import torch
 
@@ -42,6 +43,11 @@ SHAPES = {
                              shared_inter=2048),
     "h2048_maxc2": dict(hidden=2048, num_experts=16, top_k=4, moe_inter=256, shared_inter=128),
     "i1536_down_w6": dict(hidden=256, num_experts=16, top_k=4, moe_inter=1536, shared_inter=1536),
+    # BF16: gate/up tiles in two K-halves; at 3584 (28 chunks) a warp's
+    # chunks 8 + w straddle the halves
+    "h4096_khalves": dict(hidden=4096, num_experts=16, top_k=4, moe_inter=128, shared_inter=256),
+    "h3584_khalves": dict(hidden=3584, num_experts=16, top_k=4, moe_inter=256, shared_inter=128,
+                          scoring="sigmoid", routed_scaling_factor=2.5),
 }
 
 
@@ -109,8 +115,12 @@ def test_gemv_lever_ignored(fmt):
     assert torch.equal(a["out"].view(torch.int16), b["out"].view(torch.int16))
 
 
-def test_bf16_tiles_too_large_for_the_ring_are_refused():
-    shape = F("bf16", hidden=4096, num_experts=8, top_k=2, moe_inter=128, shared_inter=128)
+@pytest.mark.parametrize("variant", [
+    dict(hidden=512, moe_inter=4096, shared_inter=128),     # 32 x 4096 bf16 down tiles
+    dict(hidden=3968, moe_inter=128, shared_inter=128),     # 31 chunks: no whole K-halves
+])
+def test_bf16_tiles_too_large_for_the_ring_are_refused(variant):
+    shape = F("bf16", num_experts=8, top_k=2, **variant)
     weights, x = G.make_case(shape, 1, seed_w=241, seed_x=242)
     dl = L.DeviceLayer(weights)
     ws = L.Workspace(shape)
@@ -125,11 +135,13 @@ def test_t_layout_refused_for_fp8():
         L.DeviceLayer(weights, t_layout=True)
 
 
-# full-size shapes of the workloads in the other formats (BF16 where its
-# tiles fit the ring: hidden 2048)
+# full-size shapes of the workloads in the other formats (BF16 at hidden 4096
+# with its gate/up tiles in K-halves)
 FULL = [("decode_h2048_e128", "fp8", 1), ("decode_h2048_e128", "bf16", 1),
         ("prefill8_h2048_e512", "fp8", 8), ("prefill8_h2048_e512", "bf16", 8),
-        ("verify_h4096_e256", "fp8", 3), ("sweep_h4096_e160", "fp8", 8)]
+        ("verify_h4096_e256", "fp8", 3), ("sweep_h4096_e160", "fp8", 8),
+        ("verify_h4096_e256", "bf16", 3), ("sweep_h4096_e160", "bf16", 8),
+        ("sweep_h4096_e160", "bf16", 1)]
 
 
 @pytest.mark.parametrize("name,fmt,rows", FULL)
