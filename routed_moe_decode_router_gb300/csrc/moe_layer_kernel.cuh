@@ -387,25 +387,65 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         for (int i = 0; i < 8; ++i) wv[ri][i] = 0.f;
                     }
                 }
+                if constexpr (TK >= 2) {
+                    // wide routers (E > 256, several rows per CTA): the 32
+                    // (router row, token row) lane partials by one
+                    // reduce-scatter butterfly (31 shuffles instead of 160).
+                    // Value v = ri * 8 + r; at offset o a lane keeps the half
+                    // of its values whose bit o matches its own lane bit and
+                    // adds the partner's copy of it, so the pairs are those of
+                    // the per-value butterfly (same bits) and lane v ends
+                    // with value v.
+                    float a[kRouterRowsPerPass * kMaxRows];
 #pragma unroll
-                for (int ri = 0; ri < kRouterRowsPerPass; ++ri) {
-                    if (ri >= nr) break;
+                    for (int ri = 0; ri < kRouterRowsPerPass; ++ri)
 #pragma unroll
-                    for (int r = 0; r < kMaxRows; ++r) {
-                        if (r >= p.rows) break;
-                        const uint4 x4 = xv[r];
-                        float a = 0.f;
-                        a = fmaf(bf16_lo(x4.x), wv[ri][0], a);
-                        a = fmaf(bf16_hi(x4.x), wv[ri][1], a);
-                        a = fmaf(bf16_lo(x4.y), wv[ri][2], a);
-                        a = fmaf(bf16_hi(x4.y), wv[ri][3], a);
-                        a = fmaf(bf16_lo(x4.z), wv[ri][4], a);
-                        a = fmaf(bf16_hi(x4.z), wv[ri][5], a);
-                        a = fmaf(bf16_lo(x4.w), wv[ri][6], a);
-                        a = fmaf(bf16_hi(x4.w), wv[ri][7], a);
+                        for (int r = 0; r < kMaxRows; ++r) {
+                            const uint4 x4 = xv[r];
+                            float t = 0.f;
+                            t = fmaf(bf16_lo(x4.x), wv[ri][0], t);
+                            t = fmaf(bf16_hi(x4.x), wv[ri][1], t);
+                            t = fmaf(bf16_lo(x4.y), wv[ri][2], t);
+                            t = fmaf(bf16_hi(x4.y), wv[ri][3], t);
+                            t = fmaf(bf16_lo(x4.z), wv[ri][4], t);
+                            t = fmaf(bf16_hi(x4.z), wv[ri][5], t);
+                            t = fmaf(bf16_lo(x4.w), wv[ri][6], t);
+                            t = fmaf(bf16_hi(x4.w), wv[ri][7], t);
+                            a[ri * kMaxRows + r] = (r < p.rows) ? t : 0.f;
+                        }
 #pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-                        if (lane == 0) sm.rpart[ri][seg][r] = a;
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const bool up = (lane & o) != 0;
+#pragma unroll
+                        for (int i = 0; i < o; ++i) {
+                            const float keep = up ? a[o + i] : a[i];
+                            const float give = up ? a[i] : a[o + i];
+                            a[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+                        }
+                    }
+                    const int ri = lane / kMaxRows, r = lane % kMaxRows;
+                    if (ri < nr && r < p.rows) sm.rpart[ri][seg][r] = a[0];
+                } else {
+#pragma unroll
+                    for (int ri = 0; ri < kRouterRowsPerPass; ++ri) {
+                        if (ri >= nr) break;
+#pragma unroll
+                        for (int r = 0; r < kMaxRows; ++r) {
+                            if (r >= p.rows) break;
+                            const uint4 x4 = xv[r];
+                            float a = 0.f;
+                            a = fmaf(bf16_lo(x4.x), wv[ri][0], a);
+                            a = fmaf(bf16_hi(x4.x), wv[ri][1], a);
+                            a = fmaf(bf16_lo(x4.y), wv[ri][2], a);
+                            a = fmaf(bf16_hi(x4.y), wv[ri][3], a);
+                            a = fmaf(bf16_lo(x4.z), wv[ri][4], a);
+                            a = fmaf(bf16_hi(x4.z), wv[ri][5], a);
+                            a = fmaf(bf16_lo(x4.w), wv[ri][6], a);
+                            a = fmaf(bf16_hi(x4.w), wv[ri][7], a);
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                            if (lane == 0) sm.rpart[ri][seg][r] = a;
+                        }
                     }
                 }
             }
