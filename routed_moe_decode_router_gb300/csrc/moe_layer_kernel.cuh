@@ -387,10 +387,11 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         for (int i = 0; i < 8; ++i) wv[ri][i] = 0.f;
                     }
                 }
-                if constexpr (TK >= 2) {
-                    // wide routers (E > 256, several rows per CTA): the 32
-                    // (router row, token row) lane partials by one
-                    // reduce-scatter butterfly (31 shuffles instead of 160).
+                if (TK >= 2 || (TK == 1 && p.rows >= 2)) {
+                    // wide routers (E > 256), or two or more token rows at
+                    // E <= 256: the 32 (router row, token row) lane partials
+                    // by one reduce-scatter butterfly (31 shuffles instead of
+                    // up to 160).
                     // Value v = ri * 8 + r; at offset o a lane keeps the half
                     // of its values whose bit o matches its own lane bit and
                     // adds the partner's copy of it, so the pairs are those of
