@@ -65,6 +65,53 @@ __device__ __forceinline__ float warp_sum_compensated(float v, float c) {
     return v + c;
 }
 
+// Balanced trees over a register array (compile-time N): the largest value
+// (fmaxf skips NaN, so the result does not depend on the order), the OR of
+// bit masks, and the element at a run-time index (a select tree on its bits,
+// so no local-memory indexing).
+template <int N>
+__device__ __forceinline__ float tree_fmax(const float (&a)[N]) {
+    float t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) t[i] = a[i];
+#pragma unroll
+    for (int w = N; w > 1; w = (w + 1) / 2) {
+#pragma unroll
+        for (int i = 0; i < w / 2; ++i) t[i] = fmaxf(t[2 * i], t[2 * i + 1]);
+        if (w & 1) t[w / 2] = t[w - 1];
+    }
+    return t[0];
+}
+
+template <int N>
+__device__ __forceinline__ uint32_t tree_or(const uint32_t (&a)[N]) {
+    uint32_t t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) t[i] = a[i];
+#pragma unroll
+    for (int w = N; w > 1; w = (w + 1) / 2) {
+#pragma unroll
+        for (int i = 0; i < w / 2; ++i) t[i] = t[2 * i] | t[2 * i + 1];
+        if (w & 1) t[w / 2] = t[w - 1];
+    }
+    return t[0];
+}
+
+template <int N>
+__device__ __forceinline__ float tree_pick(const float (&a)[N], int idx) {
+    float t[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) t[i] = a[i];
+#pragma unroll
+    for (int w = N, bit = 0; w > 1; w = (w + 1) / 2, ++bit) {
+        const bool hi = (idx >> bit) & 1;
+#pragma unroll
+        for (int i = 0; i < w / 2; ++i) t[i] = hi ? t[2 * i + 1] : t[2 * i];
+        if (w & 1) t[w / 2] = t[w - 1];
+    }
+    return t[0];
+}
+
 // Each lane holds the keys of experts lane + 32 * i (i < NK * NL, so
 // E <= 32 * NK * NL) in registers, loaded once.  A selection round takes
 // every lane's best key with an fp32 max tree, the warp's best with one
@@ -104,29 +151,53 @@ __device__ __forceinline__ void warp_topk_row_nk(const float *lg, const float *b
     }
     int my_id0 = 0, my_id1 = 0;     // expert of slots lane and lane + 32
     float my_v0 = 0.f, my_v1 = 0.f; // its logit (softmax) or sigmoid (sigmoid scoring)
+    // With 16 or more candidates per lane the round's three linear chains
+    // (max, lowest matching slot, the winner's value) are balanced trees;
+    // with fewer they are short enough as they are.
+    constexpr bool kTrees = N >= 16;
     for (int j = 0; j < k; ++j) {
         // this lane's best key (a max tree, no predicates)
         float m = key[0];
+        if constexpr (kTrees) {
+            m = tree_fmax<N>(key);
+        } else {
 #pragma unroll
-        for (int i = 1; i < N; ++i) m = fmaxf(m, key[i]);
+            for (int i = 1; i < N; ++i) m = fmaxf(m, key[i]);
+        }
         // order-preserving unsigned form; an all-empty lane (NaN) maps to 0
         uint32_t u = __float_as_uint(m);
         u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
         u = (m != m) ? 0u : u;
         const uint32_t mu = __reduce_max_sync(FULL, u);
         const float mk = __uint_as_float((mu & 0x80000000u) ? (mu & 0x7fffffffu) : ~mu);
-        // the lowest expert id holding the best key (ties -> lower id)
+        // the lowest expert id holding the best key (ties -> lower id): this
+        // lane's lowest matching slot, then the warp's lowest id
         uint32_t cand = 0xffffffffu;
+        if constexpr (kTrees) {
+            uint32_t bits[N];
 #pragma unroll
-        for (int i = N - 1; i >= 0; --i) cand = key[i] == mk ? (uint32_t)(lane + 32 * i) : cand;
+            for (int i = 0; i < N; ++i) bits[i] = key[i] == mk ? (1u << i) : 0u;
+            const uint32_t hitmask = tree_or<N>(bits);
+            cand = hitmask ? (uint32_t)(lane + 32 * (__ffs(hitmask) - 1)) : 0xffffffffu;
+        } else {
+#pragma unroll
+            for (int i = N - 1; i >= 0; --i) cand = key[i] == mk ? (uint32_t)(lane + 32 * i) : cand;
+        }
         const int bi = (int)__reduce_min_sync(FULL, cand);
         // its value, from the lane that holds it; that lane retires it
         float val = 0.f;
+        if constexpr (kTrees) {
+            val = tree_pick<N>(v, bi >> 5);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const bool hit = lane + 32 * i == bi;
-            val = hit ? v[i] : val;
-            key[i] = hit ? __int_as_float(0x7fffffff) : key[i];
+            for (int i = 0; i < N; ++i)
+                key[i] = (lane + 32 * i == bi) ? __int_as_float(0x7fffffff) : key[i];
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const bool hit = lane + 32 * i == bi;
+                val = hit ? v[i] : val;
+                key[i] = hit ? __int_as_float(0x7fffffff) : key[i];
+            }
         }
         const float bv = __shfl_sync(FULL, val, bi & 31);
         if (lane == (j & 31)) {
