@@ -162,3 +162,15 @@ def test_cuda_graph_capture_matches_eager():
     for a, b in zip(eager, outs):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert ws.status() == 0
+
+
+def test_top_k_64_one_row():
+    """64 slots: the top-k warp's lanes fetch the pointer entries of slots j
+    and j + 32."""
+    shape = synth.MoeShape(hidden=512, num_experts=128, top_k=64, moe_inter=128,
+                           shared_inter=128)
+    weights, x = G.make_case(shape, 1, seed_w=191, seed_x=192)
+    res = G.gpu_run(weights, x, t_layout=True)
+    G.check_parity(weights, x, res)
+    pr = G.gpu_run(weights, x, per_row=True, t_layout=True)
+    assert torch.equal(res["out"].view(torch.int16), pr["out"].view(torch.int16))
