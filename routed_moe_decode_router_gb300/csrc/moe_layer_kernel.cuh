@@ -357,6 +357,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     // loads the token rows' inputs of its segment once, then the weights of
     // every row of the pass, all before the first use, so one memory latency
     // covers the pass.  Partial sums are added in segment order.
+    // (the one-row form's instantiations are compiled for one token row)
+    constexpr int RR = TL ? 1 : kMaxRows;
     if (is_comp) {
         const int my_rows = b < nrow ? (nrow - b + G - 1) / G : 0;
         const int nseg = (H + 255) / 256;
@@ -367,16 +369,16 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 const bool live = h0 < H;   // H is a multiple of 128, not always of 256
                 const int hc = live ? h0 : 0;
                 // every load first, from clamped addresses; unused values are zeroed after
-                uint4 xv[kMaxRows];
+                uint4 xv[RR];
 #pragma unroll
-                for (int r = 0; r < kMaxRows; ++r)
+                for (int r = 0; r < RR; ++r)
                     if (r < p.rows) xv[r] = ld_cg_v4(p.x + (size_t)r * H + hc);
                 uint4 rv[kRouterRowsPerPass];
 #pragma unroll
                 for (int ri = 0; ri < kRouterRowsPerPass; ++ri)
                     rv[ri] = router_raw(p, b + (r0 + min(ri, nr - 1)) * G, hc);
 #pragma unroll
-                for (int r = 0; r < kMaxRows; ++r)
+                for (int r = 0; r < RR; ++r)
                     if (!live || r >= p.rows) xv[r] = make_uint4(0u, 0u, 0u, 0u);
                 float wv[kRouterRowsPerPass][8];
 #pragma unroll
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         for (int i = 0; i < 8; ++i) wv[ri][i] = 0.f;
                     }
                 }
-                if (TK >= 2 || (TK == 1 && p.rows >= 2)) {
+                if (!TL && (TK >= 2 || (TK == 1 && p.rows >= 2))) {
                     // wide routers (E > 256), or two or more token rows at
                     // E <= 256: the 32 (router row, token row) lane partials
                     // by one reduce-scatter butterfly (31 shuffles instead of
@@ -402,7 +404,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     for (int ri = 0; ri < kRouterRowsPerPass; ++ri)
 #pragma unroll
                         for (int r = 0; r < kMaxRows; ++r) {
-                            const uint4 x4 = xv[r];
+                            const uint4 x4 = xv[min(r, RR - 1)];
                             float t = 0.f;
                             t = fmaf(bf16_lo(x4.x), wv[ri][0], t);
                             t = fmaf(bf16_hi(x4.x), wv[ri][1], t);
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     for (int ri = 0; ri < kRouterRowsPerPass; ++ri) {
                         if (ri >= nr) break;
 #pragma unroll
-                        for (int r = 0; r < kMaxRows; ++r) {
+                        for (int r = 0; r < RR; ++r) {
                             if (r >= p.rows) break;
                             const uint4 x4 = xv[r];
                             float a = 0.f;
