@@ -406,6 +406,63 @@ __device__ inline void build_union(const UnionSrc &src, const int32_t *s_ids, ui
     }
 }
 
+// The union of ONE row (its k <= 64 distinct top-k ids): entry p is slot p,
+// row mask 1; the same table and pointer entries build_union gives for one
+// row, without the pairwise scan (the one-row layer form, whose code is
+// kept small).  All 32 lanes of one warp call it.
+__device__ inline void build_union_one_row(const UnionSrc &src, const int32_t *s_ids,
+                                           ChunkUnion *ut, PtrEntry *ptrs, WsHeader *hdr,
+                                           int lane) {
+    const int n = src.k;
+    const moe_expert_table tb[3] = {src.gate, src.up, src.down};
+    for (int i = lane; i < kMaxIds * kMaxRows; i += 32) (&ut->uslot[0][0])[i] = 0xFF;
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int p = lane + 32 * h;
+        if (p >= n) continue;
+        const int x = s_ids[p];
+        ut->expert[p] = x;
+        ut->rowmask[p] = 1u;
+        ut->slot2u[p] = (uint8_t)p;
+        ut->uslot[p][0] = (uint8_t)p;
+        PtrEntry e;
+        if (x < 0 || x >= src.E) {
+            record_fault(hdr, MOE_DEV_BAD_EXPERT_ID, (uint32_t)p);
+            e = PtrEntry{};
+            e.expert = -1;
+        } else {
+            load_ptr_entry(tb, x, e, src.has_scales);
+            bool ok = true;
+#pragma unroll
+            for (int m = 0; m < 3; ++m) ok = ok && aligned16(e.packed[m]) && aligned16(e.scales[m]);
+            if (!ok) {
+                record_fault(hdr, MOE_DEV_MISALIGNED_PTR, (uint32_t)x);
+                e.expert = -1;
+            }
+        }
+        ptrs[p] = e;
+    }
+    if (lane == 0) {
+        if (src.has_shared) {
+            PtrEntry e;
+            const moe_nvfp4 *sm3[3] = {&src.sh_gate, &src.sh_up, &src.sh_down};
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                e.packed[m] = sm3[m]->packed;
+                e.scales[m] = sm3[m]->scales;
+                e.scale2[m] = sm3[m]->scale2;
+            }
+            e.expert = kSharedEntry;
+            ptrs[kSharedEntry] = e;
+        }
+        ut->rows = 1;
+        ut->top_k = src.k;
+        ut->per_row_mode = src.per_row_mode;
+        ut->num_union = n;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // NVFP4 x f16 MMA on one 128-input chunk of a 16-row tile
 // ---------------------------------------------------------------------------

@@ -491,7 +491,10 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
         MOE_TIC(t_union);
         UnionSrc src{E,      k,      p.rows,  p.per_row_mode, 1,       p.has_shared, FMT == 0,
                      p.gate, p.up,   p.down,  p.sh_gate,      p.sh_up, p.sh_down};
-        build_union(src, sm.ids, sm.umask, &sm.uni, sm.ptrs, hdr, lane);
+        if constexpr (TL)
+            build_union_one_row(src, sm.ids, &sm.uni, sm.ptrs, hdr, lane);
+        else
+            build_union(src, sm.ids, sm.umask, &sm.uni, sm.ptrs, hdr, lane);
         __syncwarp();
         asm volatile("bar.arrive 4, %0;" ::"r"(kLayerThreads) : "memory");
         MOE_TOC(lane == 0, 17, t_union);
