@@ -7,6 +7,9 @@ replay."""
 import pytest
 import torch
 
+import numpy as np
+
+from oracle import oracle
 from routed_moe_decode_router_gb300 import layer as L
 from routed_moe_decode_router_gb300 import native as N
 from routed_moe_decode_router_gb300 import synth
@@ -184,4 +187,24 @@ def test_cuda_graph_capture_matches_eager(fmt):
     torch.cuda.synchronize()
     for a, b in zip(eager, outs):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert ws.status() == 0
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_union_stage_with_scale_free_tables(fmt):
+    """moe_union with FP8 / BF16 expert tables, whose scale arrays are NULL:
+    the pointer entries are fetched without them, the table matches the
+    oracle's union and no fault is recorded."""
+    shape = F(fmt, num_experts=40, top_k=8)
+    weights = synth.make_layer(shape, 281, device="cuda")
+    dl = L.DeviceLayer(weights)
+    assert dl.weights.gate.scales is None or dl.weights.gate.scales == 0
+    ws = L.Workspace(shape)
+    rng = np.random.default_rng(282)
+    for rows in (1, 5, 16, 32):
+        pool = rng.choice(40, size=12, replace=False)
+        ids = np.stack([rng.choice(pool, 8, replace=False) for _ in range(rows)]).astype(np.int32)
+        uni = L.union(dl, dl.cfg, torch.from_numpy(ids).cuda(), ws)
+        G.check_union(uni, ids, 8, False, oracle.union(ids))
+    torch.cuda.synchronize()
     assert ws.status() == 0

@@ -47,6 +47,29 @@ def test_static_workspace_forward_matches_workspace_forward_twice():
         assert torch.equal(got.view(torch.int16), want.view(torch.int16))
 
 
+@pytest.mark.parametrize("case", ["t_layout_decode", "fp8_verify"])
+def test_static_workspace_other_forms(case):
+    """The static scratch also serves the t layout's fused one-row form and
+    FP8 experts: byte-identical to moe_forward with a caller workspace."""
+    import dataclasses
+    if case == "t_layout_decode":
+        shape, rows, t = synth.WORKLOADS["decode_h2048_e128"].shape, 1, True
+    else:
+        shape = dataclasses.replace(synth.WORKLOADS["verify_h4096_e256"].shape, expert_fmt="fp8")
+        rows, t = 3, False
+    weights = synth.make_layer(shape, 2100, device="cuda")
+    x = synth.make_rows(shape, rows, seed=2600, device="cuda", corr=0.7)
+    dl = L.DeviceLayer(weights, t_layout=t)
+    ws = L.Workspace(shape, t_layout=t)
+    want = L.forward(dl, x, ws)
+    assert ws.status() == 0
+    got = torch.full_like(x, float("nan"))
+    N.moe_forward_static(dl.cfg, dl.weights, x.data_ptr(), got.data_ptr(), rows,
+                         torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
 def test_static_workspace_refuses_bad_config():
     cfg = L.make_config(synth.WORKLOADS["tiny_h256_e16"].shape)
     cfg.top_k = 0
