@@ -247,12 +247,12 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     };
     // gate+up unit j (16 rows): a gate slot, then an up slot; in the t
     // layout also a slot with the unit's 16 rows of the transposed down
-    // matrix (16 x H/2 packed bytes, then the H scales of that block)
+    // matrix (16 x H/2 packed bytes, then the H scales of that block).
     // BF16 gate/up tiles too large for the ring come in two K-halves: a unit
     // is then gate half 0, up half 0, gate half 1, up half 1 (a half tile is
-    // 16 row segments of H bytes, one bulk copy each)
+    // 16 row segments of H bytes, one bulk copy each).
     const int ghalves = (FMT == 2) ? p.gu_halves : 1;
-    const int kUnitSlots = TL ? 3 : 2 * ghalves;
+    const int unit_slots = TL ? 3 : 2 * ghalves;
     const uint32_t dt_pk = kTileRows * H / 2, dt_sc = H;
     auto issue_gu = [&](int j) -> bool {
         const uint8_t *gp, *gs, *upk, *us, *dp = nullptr, *ds = nullptr;
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
             const int tile = (j - St) % It;
             if (e.expert < 0) {
                 bool ok2 = true;
-                for (int i = 0; i < kUnitSlots; ++i) ok2 = ok2 && issue_empty();
+                for (int i = 0; i < unit_slots; ++i) ok2 = ok2 && issue_empty();
                 return ok2;
             }
             gp = e.packed[0] + (size_t)tile * gu_pk;
@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
     int pj = b;   // next gate+up unit of this CTA
     if (is_prod && lane == 0) {
         pol = l2_evict_first_policy();
-        while (pj < St && pi + kUnitSlots <= S) {
+        while (pj < St && pi + unit_slots <= S) {
             issue_gu(pj);
             pj += G;
         }
