@@ -24,13 +24,17 @@ the same measurement (µs per layer-step, mean union, roofline fraction of
 the kernel alone and of the graph step) for the decode workload with
 output-major down projections, for the full sweep at one and eight rows, for
 the eight-row prefill sub-chunk with independent and with correlated rows,
-and for the decode workload with FP8 and with BF16 expert matrices.  The CPU-baseline leg times the oracle
-on all host cores and on one, and compares its outputs for the first and
-last timed layers of each workload with the GPU's (the "parity" verdicts).
+and for the decode workload with FP8 and with BF16 expert matrices; under
+"variants", for the layer's variants: an ungated and an absent shared
+expert, unnormalised top-k weights, the one-row GEMV lever, and prefill
+calls of 16 and 32 rows.  The CPU-baseline leg times the oracle on all host
+cores and on one, and compares its outputs for the first and last timed
+layers of each workload with the GPU's (the "parity" verdicts).
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -149,15 +153,17 @@ def kernel_source_hash() -> str:
 
 
 def committed_traffic(kernel: str, workload: str, rows: int, t_layout: bool = False,
-                      fmt: str = "nvfp4"):
+                      fmt: str = "nvfp4", variant: str | None = None):
     """DRAM bytes per launch of `kernel` from a committed ncu summary under
     profiles/, if it was taken on the current kernel sources (else None).
-    Lines of the t layout carry "layout=t" after the row count, and lines of
-    FP8 or BF16 experts "fmt=fp8" / "fmt=bf16" after that."""
+    Lines of the t layout carry "layout=t" after the row count, lines of FP8
+    or BF16 experts "fmt=fp8" / "fmt=bf16" after that, and lines of a layer
+    variant (another shared expert, the GEMV lever, ...) "variant=<name>"
+    after that."""
     src = kernel_source_hash()
     pat = re.compile(r"bench-traffic:\s*kernel=(\S+)\s+workload=(\S+)\s+rows=(\d+)\s+"
-                     r"(?:layout=(\w+)\s+)?(?:fmt=(\w+)\s+)?bytes_per_launch=(\d+)\s+"
-                     r"src=(\w+)")
+                     r"(?:layout=(\w+)\s+)?(?:fmt=(\w+)\s+)?(?:variant=(\S+)\s+)?"
+                     r"bytes_per_launch=(\d+)\s+src=(\w+)")
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -169,8 +175,9 @@ def committed_traffic(kernel: str, workload: str, rows: int, t_layout: bool = Fa
                 m = pat.search(line)
                 if (m and m.group(1) == kernel and m.group(2) == workload
                         and int(m.group(3)) == rows and (m.group(4) == "t") == t_layout
-                        and (m.group(5) or "nvfp4") == fmt and m.group(7) == src):
-                    return int(m.group(6))
+                        and (m.group(5) or "nvfp4") == fmt and m.group(6) == variant
+                        and m.group(8) == src):
+                    return int(m.group(7))
     return None
 
 
@@ -382,22 +389,54 @@ def time_kernels(layers, xbuf, outbuf, ws, rows, steps, stream, gemv=False):
     return kern_ms / (steps * len(layers))
 
 
+@dataclasses.dataclass(frozen=True)
+class Extra:
+    """One further measured workload: a named workload at `rows` rows over
+    `layers` layers, optionally with the activations of another workload,
+    the t layout, another expert format, the GEMV lever, or MoeShape fields
+    overridden ((name, value) pairs; `variant` names the change)."""
+    workload: str
+    rows: int
+    layers: int
+    corr_from: str | None = None
+    t_layout: bool = False
+    fmt: str = "nvfp4"
+    gemv: bool = False
+    shape: tuple = ()
+    variant: str | None = None
+
+
 # Further workloads measured beside the headline line (the metric is quoted
-# for rows = 1..8): the full sweep at one and eight rows, and the eight-row
-# prefill sub-chunk with independent and with correlated rows.  Fewer layers
-# than the full stacks, each still far more distinct weight bytes per step
-# than the 129 MB L2.
-# (workload, rows, layers, activations of another workload or None, t layout)
-# (workload, rows, layers, activations of another workload or None, t layout,
-# expert format)
+# for rows = 1..8): the decode workload with output-major down projections,
+# the full sweep at one and eight rows, the eight-row prefill sub-chunk with
+# independent and with correlated rows, and the decode workload with FP8 and
+# BF16 experts.  Fewer layers than the full stacks, each still far more
+# distinct weight bytes per step than the 129 MB L2.
 EXTRA_CONFIGS = [
-    ("decode_h2048_e128", 1, 48, None, False, "nvfp4"),
-    ("sweep_h4096_e160", 1, 16, None, True, "nvfp4"),
-    ("sweep_h4096_e160", 8, 16, None, False, "nvfp4"),
-    ("prefill8_h2048_e512", 8, 16, None, False, "nvfp4"),
-    ("prefill8_h2048_e512", 8, 16, "verify_h4096_e256", False, "nvfp4"),
-    ("decode_h2048_e128", 1, 48, None, False, "fp8"),
-    ("decode_h2048_e128", 1, 48, None, False, "bf16"),
+    Extra("decode_h2048_e128", 1, 48),
+    Extra("sweep_h4096_e160", 1, 16, t_layout=True),
+    Extra("sweep_h4096_e160", 8, 16),
+    Extra("prefill8_h2048_e512", 8, 16),
+    Extra("prefill8_h2048_e512", 8, 16, corr_from="verify_h4096_e256"),
+    Extra("decode_h2048_e128", 1, 48, fmt="fp8"),
+    Extra("decode_h2048_e128", 1, 48, fmt="bf16"),
+]
+
+# The layer's variants, each measured once: an ungated and an absent shared
+# expert and unnormalised top-k weights (decode, t layout), the one-row GEMV
+# lever (decode, output-major), and calls of 16 and 32 rows (prefill: two
+# and four 8-row sub-chunks plus the call's union; their algorithmic bytes
+# count the call's union once, while each sub-chunk sweeps its own union).
+VARIANT_CONFIGS = [
+    Extra("decode_h2048_e128", 1, 48, t_layout=True, shape=(("shared_gated", False),),
+          variant="ungated_shared"),
+    Extra("decode_h2048_e128", 1, 48, t_layout=True, shape=(("has_shared", False),),
+          variant="no_shared"),
+    Extra("decode_h2048_e128", 1, 48, t_layout=True, shape=(("norm_topk_prob", False),),
+          variant="no_norm"),
+    Extra("decode_h2048_e128", 1, 48, gemv=True, variant="gemv_lever"),
+    Extra("prefill8_h2048_e512", 16, 16, variant="rows16"),
+    Extra("prefill8_h2048_e512", 32, 8, variant="rows32"),
 ]
 
 
@@ -414,18 +453,17 @@ def use_t_layout(choice: str, rows: int) -> bool:
     return choice == "t" or (choice == "auto" and rows == 1)
 
 
-def measure_extra(name, rows, n_layers, corr_from, t_layout, fmt, steps, warmup, dev, stream,
-                  peak, nthreads, with_parity):
+def measure_extra(ex: Extra, steps, warmup, dev, stream, peak, nthreads, with_parity):
     """µs per layer-step, mean union, roofline fractions (kernel alone and
     graph step) and, on rank 0, the parity verdict of one extra workload."""
-    import dataclasses
-
     import torch
     from routed_moe_decode_router_gb300 import layer as L
     from routed_moe_decode_router_gb300 import synth
+    name, rows, n_layers, t_layout, fmt, gemv = (ex.workload, ex.rows, ex.layers, ex.t_layout,
+                                                 ex.fmt, ex.gemv)
     wl = synth.WORKLOADS[name]
-    shape = dataclasses.replace(wl.shape, expert_fmt=fmt)
-    corr = wl.corr if corr_from is None else synth.WORKLOADS[corr_from].corr
+    shape = dataclasses.replace(wl.shape, expert_fmt=fmt, **dict(ex.shape))
+    corr = wl.corr if ex.corr_from is None else synth.WORKLOADS[ex.corr_from].corr
     layers = [L.DeviceLayer(synth.make_layer(shape, wl.seed_base + l, device=dev), device=dev,
                             t_layout=t_layout) for l in range(n_layers)]
     xbuf = torch.empty((n_layers, rows, shape.hidden), dtype=torch.bfloat16, device=dev)
@@ -434,9 +472,10 @@ def measure_extra(name, rows, n_layers, corr_from, t_layout, fmt, steps, warmup,
                                   corr=corr)
     outbuf = torch.empty_like(xbuf)
     ws = L.Workspace(shape, device=dev, t_layout=t_layout)
-    _, ms, U = time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream)
+    _, ms, U = time_graph(layers, xbuf, outbuf, ws, rows, steps, warmup, stream, gemv=gemv)
     us = ms * 1000.0 / (steps * n_layers)
-    kern_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(steps, 10)), stream)
+    kern_ms = time_kernels(layers, xbuf, outbuf, ws, rows, max(1, min(steps, 10)), stream,
+                           gemv=gemv)
     bytes_per_layer = sum(layer_bytes(shape, rows, u) for u in U) / n_layers
     out = {"workload": name, "rows": rows, "layers": n_layers,
            "down_layout": "t (input-major)" if t_layout else "output-major",
@@ -448,7 +487,13 @@ def measure_extra(name, rows, n_layers, corr_from, t_layout, fmt, steps, warmup,
            "kernel_us": round(kern_ms * 1000.0, 3),
            "roofline_frac_kernel": round(bytes_per_layer / (kern_ms * 1e-3) / 1e9 / peak, 4),
            "roofline_frac_graph": round(bytes_per_layer / (us * 1e-6) / 1e9 / peak, 4),
-           "traffic": committed_traffic("moe_layer_kernel", name, rows, t_layout, fmt)}
+           "launches_per_layer": launches_per_layer(shape, rows, t_layout),
+           "traffic": committed_traffic("moe_layer_kernel", name, rows, t_layout, fmt,
+                                        ex.variant)}
+    if ex.variant:
+        out["variant"] = ex.variant
+        out["shape_changes"] = {k: v for k, v in ex.shape}
+        out["gemv_lever"] = gemv
     if with_parity:
         from oracle import oracle
         oracle.build()
@@ -588,9 +633,13 @@ def run_ours(args, rank, world, local):
     if not args.no_extra and args.workload == "decode_h2048_e128" and not args.rows \
             and not args.layers:
         line["rows_1_to_8"] = [
-            measure_extra(name, r, nl, cf, tl, fmt, args.steps, args.warmup, dev, stream, peak,
-                          os.cpu_count() or 1, do_cpu)
-            for name, r, nl, cf, tl, fmt in EXTRA_CONFIGS]
+            measure_extra(ex, args.steps, args.warmup, dev, stream, peak, os.cpu_count() or 1,
+                          do_cpu)
+            for ex in EXTRA_CONFIGS]
+        line["variants"] = [
+            measure_extra(ex, args.steps, args.warmup, dev, stream, peak, os.cpu_count() or 1,
+                          do_cpu)
+            for ex in VARIANT_CONFIGS]
     return line
 
 

@@ -115,9 +115,11 @@ enum { MOE_ROUTER_BF16 = 0, MOE_ROUTER_NVFP4 = 1 };
  * layouts above are this library's reading.  A 16-row tile of an FP8 or
  * BF16 matrix is 16*K or 32*K bytes.  BF16 gate/up tiles too large for two
  * shared-memory ring slots are streamed in two K-halves (hidden up to 4096,
- * when hidden/128 is even); configurations whose tiles still do not fit
- * (BF16 down tiles of intermediates of 2048 or more, for example) are
- * refused at the first forward (MOE_ERR_UNSUPPORTED). */
+ * when hidden/128 is even), and FP8 or BF16 down tiles too large for two
+ * slots in K-parts of whole 128-input chunks (intermediates up to 4096);
+ * configurations whose tiles still do not fit (BF16 gate/up tiles of an odd
+ * number of chunks beyond the ring, for example) are refused at the first
+ * forward (MOE_ERR_UNSUPPORTED). */
 enum { MOE_EXPERT_NVFP4 = 0, MOE_EXPERT_FP8 = 1, MOE_EXPERT_BF16 = 2 };
 
 /* One NVFP4 matrix whose pointers the host knows (router, shared expert). */

@@ -419,7 +419,7 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
                                                     : (size_t)K / 2 + (size_t)K / 16;
     };
     size_t gu_slot = (size_t)kTileRows * row_bytes(cfg->hidden);
-    const size_t d_slot = tl ? 0 : (size_t)lp.down_rows * row_bytes(L.inter_max);
+    size_t d_slot = tl ? 0 : (size_t)lp.down_rows * row_bytes(L.inter_max);
     const int budget = di->smem_optin - 1024;
     // BF16 gate/up tiles that do not fit two ring slots are taken in two
     // K-halves (each half a whole number of 128-input chunks)
@@ -428,6 +428,22 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
         (cfg->hidden / kChunk) % 2 == 0) {
         lp.gu_halves = 2;
         gu_slot /= 2;
+    }
+    // FP8 / BF16 down tiles that do not fit two ring slots are taken in
+    // K-parts of down_pc chunks (down_rows row segments per slot), as many
+    // chunks per part as leave room for four slots
+    lp.down_pc = L.inter_max / kChunk;
+    if (cfg->expert_fmt != MOE_EXPERT_NVFP4 && !tl &&
+        layer_smem_bytes(2, (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot)) > (size_t)budget) {
+        const size_t per_chunk = (size_t)lp.down_rows * row_bytes(kChunk);
+        int pc = lp.down_pc;
+        while (pc > 1 && layer_smem_bytes(4, (uint32_t)(gu_slot > per_chunk * pc ? gu_slot
+                                                                          : per_chunk * pc)) >
+                             (size_t)budget)
+            --pc;
+        if (wide) return fail(MOE_ERR_UNSUPPORTED, "wide down units do not fit the ring");
+        lp.down_pc = pc;
+        d_slot = per_chunk * pc;
     }
     lp.slot_bytes = (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot);
     int S = 16;

@@ -560,11 +560,28 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     const int tile = (j - Sd) % Hd;
                     if (e.expert < 0) {
                         ok = issue_empty();
+                        if constexpr (FMT != 0)
+                            for (int c0 = p.down_pc; ok && c0 < p.I / kChunk; c0 += p.down_pc)
+                                ok = issue_empty();
                         continue;
                     }
                     K = p.I;
                     dp = e.packed[2] + (size_t)tile * DR * fmt_row_bytes<FMT>(K);
                     ds = e.scales[2] + (size_t)tile * DR * fmt_scale_row_bytes<FMT>(K);
+                }
+                if constexpr (FMT != 0) {
+                    // FP8 / BF16 down unit in K-parts of down_pc chunks: DR
+                    // row segments per slot
+                    const int nch = K / kChunk;
+                    if (nch > p.down_pc) {
+                        for (int c0 = 0; ok && c0 < nch; c0 += p.down_pc) {
+                            const int nc = min(p.down_pc, nch - c0);
+                            if (!(ok = acquire(pi))) break;
+                            issue_rows(dp + fmt_row_bytes<FMT>(c0 * kChunk), fmt_row_bytes<FMT>(K),
+                                       fmt_row_bytes<FMT>(nc * kChunk), DR);
+                        }
+                        continue;
+                    }
                 }
                 if (!(ok = acquire(pi))) break;
                 issue_pair(dp, ds, DR * fmt_row_bytes<FMT>(K), DR * fmt_scale_row_bytes<FMT>(K));
@@ -1141,6 +1158,55 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                              wide ? nch : (split ? 4 : kConsumerWarps), lane, bh, inv0, inv1);
                 MOE_TOC(tid == 0, 21, t_b);
                 for (; j < jend; ++j) {
+                    if constexpr (FMT != 0) {
+                        // FP8 / BF16 down unit in K-parts of down_pc chunks,
+                        // one slot each (DR row segments): this warp's chunks
+                        // in the same order as from a whole tile
+                        if (nch > p.down_pc) {
+                            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
+                            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+                            for (int k0 = 0; k0 < nch; k0 += p.down_pc) {
+                                const int nc = min(p.down_pc, nch - k0);
+                                const int segb = (int)fmt_row_bytes<FMT>(nc * kChunk);
+                                const int s = rs;
+                                const uint32_t par = rp;
+                                next_slot();
+                                const bool ok = ring_wait(&full[s], par, abort, hdr, (uint32_t)ci);
+                                const uint8_t *st = ring + (size_t)s * p.slot_bytes;
+                                if (ok) {
+#pragma unroll
+                                    for (int m = 0; m < MC_D; ++m) {
+                                        const int c = split ? cw + 4 * m : warp + kConsumerWarps * m;
+                                        if (c < k0 || c >= k0 + nc) continue;
+                                        if (split) {
+                                            chunk_mma_t<FMT>(st + gw * kTileRows * segb, st, segb, 0,
+                                                             c - k0, g, q, bh[m], a0, a1);
+                                        } else {
+                                            chunk_mma_t<FMT>(st, st, segb, 0, c - k0, g, q, bh[m], a0, a1);
+                                            chunk_mma_t<FMT>(st + kTileRows * segb, st, segb, 0, c - k0, g,
+                                                             q, bh[m], c0, c1);
+                                        }
+                                    }
+                                }
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&empty[s]);
+                                ++ci;
+                            }
+                            float da[4], dc[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                da[i] = a0[i] + a1[i];
+                                dc[i] = c0[i] + c1[i];
+                            }
+                            const int rb = claim_red();
+                            store_partial(sm.red[rb][warp], da, g, q, inv0, inv1);
+                            store_partial(sm.red[rb][warp] + 128, dc, g, q, inv0, inv1);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&sm.red_full[rb]);
+                            ++ui;
+                            continue;
+                        }
+                    }
                     const int s = rs;
                     const uint32_t par = rp;
                     next_slot();

@@ -183,6 +183,8 @@ struct LayerParams {
     int down_rows;          // output rows of a down unit: 32, or 64 (wide units)
     int down_split;         // 32-row units whose 8, 12 or 16 chunks go four to a tile
     int gu_halves;          // 2: BF16 gate/up tiles in two K-halves (one ring slot each)
+    int down_pc;            // 128-input chunks of a down unit per ring slot (FP8 / BF16
+                            // down units of more chunks come in K-parts, one slot each)
     const uint16_t *x;
     uint16_t *out;
     const uint16_t *router_bf16;

@@ -172,13 +172,19 @@ def test_committed_traffic_keyed_to_kernel_workload_rows_and_sources(tmp_path, m
         "text\nbench-traffic: kernel=moe_layer_kernel workload=decode_h2048_e128 rows=1 "
         "bytes_per_launch=24182016 src=abc123\n"
         "bench-traffic: kernel=moe_layer_kernel workload=decode_h2048_e128 rows=1 layout=t "
-        "bytes_per_launch=24100000 src=abc123\n")
+        "bytes_per_launch=24100000 src=abc123\n"
+        "bench-traffic: kernel=moe_layer_kernel workload=decode_h2048_e128 rows=1 layout=t "
+        "variant=no_shared bytes_per_launch=21500000 src=abc123\n")
     (tmp_path / "profiles" / "raw.ncu-rep").write_text(
         "bench-traffic: kernel=moe_layer_kernel workload=w rows=1 bytes_per_launch=1 src=abc123\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "kernel_source_hash", lambda: "abc123")
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1) == 24182016
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1, True) == 24100000
+    assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1, True, "nvfp4",
+                                   "no_shared") == 21500000
+    assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1, True, "nvfp4",
+                                   "ungated_shared") is None
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 1, False, "fp8") is None
     assert bench.committed_traffic("moe_layer_kernel", "decode_h2048_e128", 8) is None
     assert bench.committed_traffic("moe_layer_kernel", "prefill8_h2048_e512", 1) is None
@@ -262,3 +268,30 @@ def test_launches_per_layer():
     assert bench.launches_per_layer(dec, 8, False) == 1
     assert bench.launches_per_layer(dec, 16, False) == 3  # two sub-chunks + the union kernel
     assert bench.launches_per_layer(dec, 3, True) == 4    # one launch per row + the union
+
+
+def test_extra_and_variant_configs_are_well_formed():
+    """Every further measured workload names a known workload, a row count the
+    library takes (at most 32 rows, rows * top_k <= 256), real MoeShape
+    fields, and enough layers that one step streams more distinct weight
+    bytes than the 129 MB L2 (so no flush is needed between steps)."""
+    import dataclasses
+
+    import bench
+    from routed_moe_decode_router_gb300 import synth
+    fields = {f.name for f in dataclasses.fields(synth.MoeShape)}
+    names = set()
+    for ex in bench.EXTRA_CONFIGS + bench.VARIANT_CONFIGS:
+        wl = synth.WORKLOADS[ex.workload]
+        assert all(k in fields for k, _ in ex.shape)
+        shape = dataclasses.replace(wl.shape, expert_fmt=ex.fmt, **dict(ex.shape))
+        assert 1 <= ex.rows <= 32 and ex.rows * shape.top_k <= 256
+        assert not (ex.t_layout and ex.fmt != "nvfp4")
+        weights = ex.layers * (bench.layer_bytes(shape, ex.rows, shape.top_k)
+                               - 2 * ex.rows * shape.hidden * 2)
+        assert weights > 129e6, ex
+        key = (ex.workload, ex.rows, ex.t_layout, ex.fmt, ex.gemv, ex.shape, ex.corr_from)
+        assert key not in names
+        names.add(key)
+    assert all(ex.variant for ex in bench.VARIANT_CONFIGS)
+    assert not any(ex.variant for ex in bench.EXTRA_CONFIGS)

@@ -1,8 +1,9 @@
 """FP8 and BF16 expert matrices on the GPU: oracle parity (the oracle decodes
 the same bytes in its own code), union mode byte-identical to per-row mode,
 calls of several sub-chunks, degenerate routings, BF16 gate/up tiles taken in
-two K-halves (hidden 3584 and 4096), the full-size shapes, the refusal of
-BF16 down tiles that do not fit the shared-memory ring, and CUDA-graph
+two K-halves (hidden 3584 and 4096), BF16 down tiles in K-parts
+(intermediates of 2048 to 4096), the full-size shapes, the refusal of BF16
+gate/up tiles that do not fit the shared-memory ring, and CUDA-graph
 replay."""
 import pytest
 import torch
@@ -51,11 +52,15 @@ SHAPES = {
     "h4096_khalves": dict(hidden=4096, num_experts=16, top_k=4, moe_inter=128, shared_inter=256),
     "h3584_khalves": dict(hidden=3584, num_experts=16, top_k=4, moe_inter=256, shared_inter=128,
                           scoring="sigmoid", routed_scaling_factor=2.5),
+    # BF16: down units in K-parts of 6 chunks (four 48 KB slots at hidden
+    # 512): 32 chunks in parts of 6, 6, 6, 6, 6, 2 beside a 1-chunk shared
+    # expert; 18 chunks in three parts; split units of 16 chunks (parts 6,
+    # 6, 4) beside split units of 12
+    "i4096_dparts": dict(hidden=512, num_experts=16, top_k=4, moe_inter=4096, shared_inter=128),
+    "i2304_dparts": dict(hidden=512, num_experts=12, top_k=3, moe_inter=2304, shared_inter=2304),
+    "split_dparts": dict(hidden=512, num_experts=16, top_k=2, moe_inter=2048, shared_inter=1536,
+                         scoring="sigmoid", routed_scaling_factor=1.5),
 }
-
-
-# BF16 down tiles of 32 rows x 2048 inputs (128 KB) do not fit two ring slots
-REFUSED = {("bf16", "split_down_mixed")}
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
@@ -67,11 +72,6 @@ def test_small_shapes_vs_oracle(fmt, name, rows):
     corr = 0.7 if shape.scoring == "sigmoid" else None
     weights, x = G.make_case(shape, rows, seed_w=201, seed_x=202, corr=corr)
     dl = L.DeviceLayer(weights)
-    if (fmt, name) in REFUSED:
-        with pytest.raises(N.MoeError) as ei:
-            L.forward(dl, x, L.Workspace(shape))
-        assert ei.value.status == 2 and "shared memory" in str(ei.value)
-        return
     res = G.gpu_run(weights, x, dl=dl)
     G.check_parity(weights, x, res)
     pr = G.gpu_run(weights, x, per_row=True, dl=dl)
@@ -119,7 +119,6 @@ def test_gemv_lever_ignored(fmt):
 
 
 @pytest.mark.parametrize("variant", [
-    dict(hidden=512, moe_inter=4096, shared_inter=128),     # 32 x 4096 bf16 down tiles
     dict(hidden=3968, moe_inter=128, shared_inter=128),     # 31 chunks: no whole K-halves
 ])
 def test_bf16_tiles_too_large_for_the_ring_are_refused(variant):

@@ -29,13 +29,13 @@ def built():
 
 def draw(seed: int):
     """(shape, rows, t_layout, gemv, corr) of case `seed`; all within the
-    library's limits (BF16 down tiles of at most 1024-wide intermediates)."""
+    library's limits (FP8 / BF16 down tiles beyond the ring come in K-parts)."""
     rnd = random.Random(1000 + seed)
     fmt = rnd.choice(["nvfp4", "nvfp4", "fp8", "bf16"])
     H = rnd.choice([128, 256, 384, 512, 768, 1024, 2048])
     E = rnd.choice([1, 2, 5, 8, 16, 24, 40, 64, 100, 128, 160, 256, 300, 512])
     k = rnd.randint(1, min(E, 16))
-    widths = [128, 256, 384, 512, 768, 1024] + ([] if fmt == "bf16" else [1536, 2048])
+    widths = [128, 256, 384, 512, 768, 1024, 1536, 2048]
     I, Is = rnd.choice(widths), rnd.choice(widths)
     sigm = rnd.random() < 0.4
     shape = synth.MoeShape(
