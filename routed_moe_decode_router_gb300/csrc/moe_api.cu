@@ -434,7 +434,8 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     // chunks per part as leave room for four slots
     lp.down_pc = L.inter_max / kChunk;
     if (cfg->expert_fmt != MOE_EXPERT_NVFP4 && !tl &&
-        layer_smem_bytes(2, (uint32_t)(gu_slot > d_slot ? gu_slot : d_slot)) > (size_t)budget) {
+        layer_smem_bytes(2, (uint32_t)gu_slot) <= (size_t)budget &&
+        layer_smem_bytes(2, (uint32_t)d_slot) > (size_t)budget) {
         const size_t per_chunk = (size_t)lp.down_rows * row_bytes(kChunk);
         int pc = lp.down_pc;
         while (pc > 1 && layer_smem_bytes(4, (uint32_t)(gu_slot > per_chunk * pc ? gu_slot
@@ -458,6 +459,8 @@ static moe_status forward_impl(const moe_config *cfg, const moe_weights *w,
     const int mc_gu = (cfg->hidden / kChunk + kConsumerWarps - 1) / kConsumerWarps;
     const int mc_d = lp.down_split ? L.inter_max / kChunk / 4
                                    : (L.inter_max / kChunk + kConsumerWarps - 1) / kConsumerWarps;
+    if (lp.down_pc < L.inter_max / kChunk && !down_parts_possible(cfg->expert_fmt, mc_d))
+        return fail(MOE_ERR_UNSUPPORTED, "down tiles in K-parts need more chunks per warp");
 
     // one launch per sub-chunk of at most 8 rows (64 ids), in row order; a
     // call of several sub-chunks then resolves the union of all its rows

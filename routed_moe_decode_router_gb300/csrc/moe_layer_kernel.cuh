@@ -163,6 +163,7 @@ __device__ __forceinline__ void router_decode(const LayerParams &p, int row, uin
 template <int MC_GU, int MC_D, int TK, bool GV, bool TL, int FMT = 0>
 __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const LayerParams p) {
     static_assert(FMT == 0 || (!GV && !TL), "GEMV variant and t layout: NVFP4 experts only");
+    constexpr bool kDownParts = down_parts_possible(FMT, MC_D);
     extern __shared__ __align__(128) uint8_t smem[];
     LayerSmem &sm = *reinterpret_cast<LayerSmem *>(smem);
     uint8_t *ring = smem + kLayerSmemFixed;
@@ -560,7 +561,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     const int tile = (j - Sd) % Hd;
                     if (e.expert < 0) {
                         ok = issue_empty();
-                        if constexpr (FMT != 0)
+                        if constexpr (kDownParts)
                             for (int c0 = p.down_pc; ok && c0 < p.I / kChunk; c0 += p.down_pc)
                                 ok = issue_empty();
                         continue;
@@ -569,7 +570,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                     dp = e.packed[2] + (size_t)tile * DR * fmt_row_bytes<FMT>(K);
                     ds = e.scales[2] + (size_t)tile * DR * fmt_scale_row_bytes<FMT>(K);
                 }
-                if constexpr (FMT != 0) {
+                if constexpr (kDownParts) {
                     // FP8 / BF16 down unit in K-parts of down_pc chunks: DR
                     // row segments per slot
                     const int nch = K / kChunk;
@@ -1158,7 +1159,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                              wide ? nch : (split ? 4 : kConsumerWarps), lane, bh, inv0, inv1);
                 MOE_TOC(tid == 0, 21, t_b);
                 for (; j < jend; ++j) {
-                    if constexpr (FMT != 0) {
+                    if constexpr (kDownParts) {
                         // FP8 / BF16 down unit in K-parts of down_pc chunks,
                         // one slot each (DR row segments): this warp's chunks
                         // in the same order as from a whole tile

@@ -173,6 +173,15 @@ struct UnionParams {
 // rows, the call's rows row_base .. row_base + rows - 1.  publish_union: the
 // call has only this sub-chunk, so its union is the call's (written to the
 // workspace for moe_read_routing).
+// Whether a down unit of a layer-kernel instantiation (expert format fmt,
+// MC_D B-fragment chunks per warp) can need K-parts, i.e. an FP8 / BF16
+// down tile of 32 rows that does not fit two ring slots: BF16 from 13
+// chunks (MC_D >= 2), FP8 from 26 chunks (MC_D = 4).  The other
+// instantiations carry no K-part code.
+__host__ __device__ constexpr bool down_parts_possible(int fmt, int mc_d) {
+    return fmt == 2 ? mc_d >= 2 : (fmt == 1 && mc_d == 4);
+}
+
 struct LayerParams {
     int H, E, k, rows, I, Is;
     int row_base, publish_union;
