@@ -164,6 +164,12 @@ template <int MC_GU, int MC_D, int TK, bool GV, bool TL, int FMT = 0>
 __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const LayerParams p) {
     static_assert(FMT == 0 || (!GV && !TL), "GEMV variant and t layout: NVFP4 experts only");
     constexpr bool kDownParts = down_parts_possible(FMT, MC_D);
+    // one-row form with 4 chunks per warp (hidden 3200 .. 4096, a ring of 5
+    // to 7 slots): each unit's gate slot is released before its up slot is
+    // waited for, which keeps one more slot in flight; the other
+    // instantiations multiply gate and up chunks interleaved (two independent
+    // chains), which the multi-row sweeps need
+    constexpr bool kGateFirst = TL && MC_GU == 4;
     extern __shared__ __align__(128) uint8_t smem[];
     LayerSmem &sm = *reinterpret_cast<LayerSmem *>(smem);
     uint8_t *ring = smem + kLayerSmemFixed;
@@ -970,7 +976,8 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                 }
                 MOE_TIC(t_w);
                 const bool ok0 = ring_wait(&full[s0], p0, abort, hdr, (uint32_t)ci);
-                const bool ok1 = ring_wait(&full[s1], p1, abort, hdr, (uint32_t)ci + 1);
+                bool ok1 = true;
+                if constexpr (!kGateFirst) ok1 = ring_wait(&full[s1], p1, abort, hdr, (uint32_t)ci + 1);
                 MOE_TOC(tid == 0, 18, t_w);
                 MOE_TIC(t_c);
                 const uint8_t *sg = ring + (size_t)s0 * p.slot_bytes;
@@ -1024,6 +1031,48 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         mbar_arrive(&empty[s3h]);
                     }
                     ci += 2;
+                } else if constexpr (kGateFirst) {
+                    // the gate chunks first; the gate slot goes back to the
+                    // producer before the up slot is waited for
+                    if (ok0) {
+#pragma unroll
+                        for (int m = 0; m < MC_GU; ++m) {
+                            const int c = warp + kConsumerWarps * m;
+                            if (c < nch) {
+                                if constexpr (GV) {
+                                    float ga, gb;
+                                    chunk_gemv(sg, sg + gu_pk, H / 2, H / 16, c, g, q, bx[m], ga, gb);
+                                    dg0[0] += ga;
+                                    dg0[2] += gb;
+                                } else {
+                                    chunk_mma_t<FMT>(sg, sg + gu_pk, fmt_row_bytes<FMT>(H),
+                                                     fmt_scale_row_bytes<FMT>(H), c, g, q, bx[m], dg0, dg1);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s0]);
+                    ok1 = ring_wait(&full[s1], p1, abort, hdr, (uint32_t)ci + 1);
+                    if (ok1) {
+#pragma unroll
+                        for (int m = 0; m < MC_GU; ++m) {
+                            const int c = warp + kConsumerWarps * m;
+                            if (c < nch) {
+                                if constexpr (GV) {
+                                    float ua, ub;
+                                    chunk_gemv(su, su + gu_pk, H / 2, H / 16, c, g, q, bx[m], ua, ub);
+                                    du0[0] += ua;
+                                    du0[2] += ub;
+                                } else {
+                                    chunk_mma_t<FMT>(su, su + gu_pk, fmt_row_bytes<FMT>(H),
+                                                     fmt_scale_row_bytes<FMT>(H), c, g, q, bx[m], du0, du1);
+                                }
+                            }
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[s1]);
                 } else if (ok0 && ok1) {
 #pragma unroll
                     for (int m = 0; m < MC_GU; ++m) {
@@ -1046,7 +1095,7 @@ __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const Layer
                         }
                     }
                 }
-                if (!(FMT == 2 && ghalves == 2)) {
+                if (!(FMT == 2 && ghalves == 2) && !kGateFirst) {
                     __syncwarp();
                     if (lane == 0) {
                         mbar_arrive(&empty[s0]);
