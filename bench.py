@@ -424,7 +424,7 @@ EXTRA_CONFIGS = [
 
 # The layer's variants, each measured once: an ungated and an absent shared
 # expert and unnormalised top-k weights (decode, t layout), the one-row GEMV
-# lever (decode, output-major), and calls of 16 and 32 rows (prefill: two
+# lever (decode, both layouts), and calls of 16 and 32 rows (prefill: two
 # and four 8-row sub-chunks plus the call's union; their algorithmic bytes
 # count the call's union once, while each sub-chunk sweeps its own union).
 VARIANT_CONFIGS = [
@@ -435,6 +435,7 @@ VARIANT_CONFIGS = [
     Extra("decode_h2048_e128", 1, 48, t_layout=True, shape=(("norm_topk_prob", False),),
           variant="no_norm"),
     Extra("decode_h2048_e128", 1, 48, gemv=True, variant="gemv_lever"),
+    Extra("decode_h2048_e128", 1, 48, t_layout=True, gemv=True, variant="gemv_lever_t"),
     Extra("prefill8_h2048_e512", 16, 16, variant="rows16"),
     Extra("prefill8_h2048_e512", 32, 8, variant="rows32"),
 ]
