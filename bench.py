@@ -22,14 +22,15 @@ projections in the t layout (the fused one-row form; --down-layout picks the
 layout, "auto" = t for one-row workloads).  Beside it, under "rows_1_to_8",
 the same measurement (µs per layer-step, mean union, roofline fraction of
 the kernel alone and of the graph step) for the decode workload with
-output-major down projections, for the full sweep at one and eight rows, for
-the eight-row prefill sub-chunk with independent and with correlated rows,
-and for the decode workload with FP8 and with BF16 expert matrices; under
-"variants", for the layer's variants: an ungated and an absent shared
-expert, unnormalised top-k weights, the one-row GEMV lever, and prefill
-calls of 16 and 32 rows.  The CPU-baseline leg times the oracle on all host
-cores and on one, and compares its outputs for the first and last timed
-layers of each workload with the GPU's (the "parity" verdicts).
+output-major down projections and with FP8 and BF16 expert matrices, for
+the full sweep at every row count 1..8, for the speculative-verify rows 2, 3
+and 4, and for the eight-row prefill sub-chunk with independent and with
+correlated rows; under "variants", for the layer's variants: prefill calls
+of 16 and 32 rows, an ungated and an absent shared expert, unnormalised
+top-k weights, and the one-row GEMV lever.  The CPU-baseline leg times the
+oracle on all host cores and on one, and compares its outputs for the first
+and last timed layers of each workload with the GPU's (the "parity"
+verdicts).
 """
 from __future__ import annotations
 
@@ -407,20 +408,21 @@ class Extra:
 
 
 # Further workloads measured beside the headline line (the metric is quoted
-# for rows = 1..8): the decode workload with output-major down projections,
-# the full sweep at one and eight rows, the eight-row prefill sub-chunk with
-# independent and with correlated rows, and the decode workload with FP8 and
-# BF16 experts.  Fewer layers than the full stacks, each still far more
-# distinct weight bytes per step than the 129 MB L2.
-EXTRA_CONFIGS = [
-    Extra("decode_h2048_e128", 1, 48),
-    Extra("sweep_h4096_e160", 1, 16, t_layout=True),
-    Extra("sweep_h4096_e160", 8, 16),
-    Extra("prefill8_h2048_e512", 8, 16),
-    Extra("prefill8_h2048_e512", 8, 16, corr_from="verify_h4096_e256"),
-    Extra("decode_h2048_e128", 1, 48, fmt="fp8"),
-    Extra("decode_h2048_e128", 1, 48, fmt="bf16"),
-]
+# for rows = 1..8): the decode workload with output-major down projections
+# and with FP8 and BF16 experts, the full sweep at every row count 1..8, the
+# speculative-verify rows 2, 3 and 4, and the eight-row prefill sub-chunk
+# with independent and with correlated rows.  Fewer layers than the full
+# stacks, each still far more distinct weight bytes per step than the
+# 129 MB L2.  Consecutive lines of the same layer stack share one build.
+EXTRA_CONFIGS = (
+    [Extra("decode_h2048_e128", 1, 48),
+     Extra("decode_h2048_e128", 1, 48, fmt="fp8"),
+     Extra("decode_h2048_e128", 1, 48, fmt="bf16"),
+     Extra("sweep_h4096_e160", 1, 16, t_layout=True)]
+    + [Extra("sweep_h4096_e160", r, 16) for r in range(2, 9)]
+    + [Extra("verify_h4096_e256", r, 16) for r in (2, 3, 4)]
+    + [Extra("prefill8_h2048_e512", 8, 16),
+       Extra("prefill8_h2048_e512", 8, 16, corr_from="verify_h4096_e256")])
 
 # The layer's variants, each measured once: an ungated and an absent shared
 # expert and unnormalised top-k weights (decode, t layout), the one-row GEMV
@@ -428,6 +430,8 @@ EXTRA_CONFIGS = [
 # and four 8-row sub-chunks plus the call's union; their algorithmic bytes
 # count the call's union once, while each sub-chunk sweeps its own union).
 VARIANT_CONFIGS = [
+    Extra("prefill8_h2048_e512", 16, 16, variant="rows16"),
+    Extra("prefill8_h2048_e512", 32, 8, variant="rows32"),
     Extra("decode_h2048_e128", 1, 48, t_layout=True, shape=(("shared_gated", False),),
           variant="ungated_shared"),
     Extra("decode_h2048_e128", 1, 48, t_layout=True, shape=(("has_shared", False),),
@@ -436,8 +440,6 @@ VARIANT_CONFIGS = [
           variant="no_norm"),
     Extra("decode_h2048_e128", 1, 48, gemv=True, variant="gemv_lever"),
     Extra("decode_h2048_e128", 1, 48, t_layout=True, gemv=True, variant="gemv_lever_t"),
-    Extra("prefill8_h2048_e512", 16, 16, variant="rows16"),
-    Extra("prefill8_h2048_e512", 32, 8, variant="rows32"),
 ]
 
 
@@ -454,9 +456,12 @@ def use_t_layout(choice: str, rows: int) -> bool:
     return choice == "t" or (choice == "auto" and rows == 1)
 
 
-def measure_extra(ex: Extra, steps, warmup, dev, stream, peak, nthreads, with_parity):
+def measure_extra(ex: Extra, steps, warmup, dev, stream, peak, nthreads, with_parity,
+                  cache=None):
     """µs per layer-step, mean union, roofline fractions (kernel alone and
-    graph step) and, on rank 0, the parity verdict of one extra workload."""
+    graph step) and, on rank 0, the parity verdict of one extra workload.
+    `cache` (a dict) keeps the last layer stack for the next line of the
+    same stack."""
     import torch
     from routed_moe_decode_router_gb300 import layer as L
     from routed_moe_decode_router_gb300 import synth
@@ -465,8 +470,15 @@ def measure_extra(ex: Extra, steps, warmup, dev, stream, peak, nthreads, with_pa
     wl = synth.WORKLOADS[name]
     shape = dataclasses.replace(wl.shape, expert_fmt=fmt, **dict(ex.shape))
     corr = wl.corr if ex.corr_from is None else synth.WORKLOADS[ex.corr_from].corr
-    layers = [L.DeviceLayer(synth.make_layer(shape, wl.seed_base + l, device=dev), device=dev,
-                            t_layout=t_layout) for l in range(n_layers)]
+    cache = {} if cache is None else cache
+    key = (name, fmt, t_layout, ex.shape, n_layers)
+    if cache.get("key") != key:
+        cache.clear()
+        torch.cuda.empty_cache()
+        cache["layers"] = [L.DeviceLayer(synth.make_layer(shape, wl.seed_base + l, device=dev),
+                                         device=dev, t_layout=t_layout) for l in range(n_layers)]
+        cache["key"] = key
+    layers = cache["layers"]
     xbuf = torch.empty((n_layers, rows, shape.hidden), dtype=torch.bfloat16, device=dev)
     for l in range(n_layers):
         xbuf[l] = synth.make_rows(shape, rows, seed=wl.seed_base + 500 + l, device=dev,
@@ -506,7 +518,6 @@ def measure_extra(ex: Extra, steps, warmup, dev, stream, peak, nthreads, with_pa
     if ws.status() != 0:
         raise RuntimeError("device status set while timing %s" % name)
     del layers, xbuf, outbuf, ws
-    torch.cuda.empty_cache()
     return out
 
 
@@ -633,14 +644,17 @@ def run_ours(args, rank, world, local):
     torch.cuda.empty_cache()
     if not args.no_extra and args.workload == "decode_h2048_e128" and not args.rows \
             and not args.layers:
+        cache = {}
         line["rows_1_to_8"] = [
             measure_extra(ex, args.steps, args.warmup, dev, stream, peak, os.cpu_count() or 1,
-                          do_cpu)
+                          do_cpu, cache)
             for ex in EXTRA_CONFIGS]
         line["variants"] = [
             measure_extra(ex, args.steps, args.warmup, dev, stream, peak, os.cpu_count() or 1,
-                          do_cpu)
+                          do_cpu, cache)
             for ex in VARIANT_CONFIGS]
+        cache.clear()
+        torch.cuda.empty_cache()
     return line
 
 
