@@ -5,7 +5,8 @@
 // projections), moe_layer_tk0_gv.cu .. moe_layer_tk3_gv.cu (the one-row
 // CUDA-core GEMV), moe_layer_tk0_t.cu .. moe_layer_tk3_t.cu (the fused
 // one-row form for down projections in the t layout, both variants) and
-// moe_layer_tk*_f8.cu / moe_layer_tk*_bf.cu (FP8 and BF16 expert matrices).
+// moe_layer_tk*_f8.cu / moe_layer_tk*_bf.cu (FP8 and BF16 expert matrices)
+// and moe_layer_tk*_kp.cu (FP8 / BF16 with down tiles in K-parts).
 #include <cuda_runtime.h>
 
 #include "moe_layout.h"
@@ -32,6 +33,10 @@ void *layer_kernel_tk0_t(int mc_gu, bool gv);
 void *layer_kernel_tk1_t(int mc_gu, bool gv);
 void *layer_kernel_tk2_t(int mc_gu, bool gv);
 void *layer_kernel_tk3_t(int mc_gu, bool gv);
+void *layer_kernel_tk0_kp(int fmt, int mc_gu, int mc_d);
+void *layer_kernel_tk1_kp(int fmt, int mc_gu, int mc_d);
+void *layer_kernel_tk2_kp(int fmt, int mc_gu, int mc_d);
+void *layer_kernel_tk3_kp(int fmt, int mc_gu, int mc_d);
 size_t layer_fixed_smem_bytes();
 
 size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
@@ -42,7 +47,16 @@ size_t layer_smem_bytes(int stages, uint32_t slot_bytes) {
 // in registers: 4, 8, 16 or two lists of 16).
 static int topk_class(int E) { return E <= 128 ? 0 : (E <= 256 ? 1 : (E <= 512 ? 2 : 3)); }
 
-static void *layer_kernel(int mc_gu, int mc_d, int tk, bool gv, bool tl, int fmt) {
+static void *layer_kernel(int mc_gu, int mc_d, int tk, bool gv, bool tl, int fmt,
+                          bool kp = false) {
+    if (kp) {
+        switch (tk) {
+        case 0: return layer_kernel_tk0_kp(fmt, mc_gu, mc_d);
+        case 1: return layer_kernel_tk1_kp(fmt, mc_gu, mc_d);
+        case 2: return layer_kernel_tk2_kp(fmt, mc_gu, mc_d);
+        default: return layer_kernel_tk3_kp(fmt, mc_gu, mc_d);
+        }
+    }
     if (fmt == MOE_EXPERT_FP8) {
         switch (tk) {
         case 0: return layer_kernel_tk0_f8(mc_gu, mc_d);
@@ -96,13 +110,22 @@ cudaError_t set_layer_smem_limit(int bytes) {
                                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                          bytes);
                     if (e != cudaSuccess) return e;
+                    void *kp = layer_kernel(a, b, t, false, false, f, true);
+                    if (kp) {
+                        e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+                        if (e != cudaSuccess) return e;
+                    }
                 }
     return cudaSuccess;
 }
 
 cudaError_t launch_layer(const LayerParams &p, int grid, size_t smem, int mc_gu, int mc_d,
                          bool gemv, bool t_layout, int expert_fmt, cudaStream_t stream) {
-    void *fn = layer_kernel(mc_gu, mc_d, topk_class(p.E), gemv, t_layout, expert_fmt);
+    // FP8 / BF16 down tiles in K-parts (down_pc below the widest
+    // intermediate's chunk count) take the K-part instantiations
+    const int inter_max = p.has_shared && p.Is > p.I ? p.Is : p.I;
+    const bool kp = !t_layout && expert_fmt != MOE_EXPERT_NVFP4 && p.down_pc < inter_max / kChunk;
+    void *fn = layer_kernel(mc_gu, mc_d, topk_class(p.E), gemv, t_layout, expert_fmt, kp);
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -159,11 +159,15 @@ __device__ __forceinline__ void router_decode(const LayerParams &p, int row, uin
 // (chunk_gemv) instead of the tensor-core MMA (chunk_mma); TL: the fused
 // one-row form for down projections in the t layout (MC_D unused); FMT: the
 // expert format (0 NVFP4, 1 FP8, 2 BF16; the GEMV variant and the t layout
-// exist for NVFP4 only).
-template <int MC_GU, int MC_D, int TK, bool GV, bool TL, int FMT = 0>
+// exist for NVFP4 only); KP: the FP8 / BF16 instantiations whose down units
+// come in K-parts (down tiles beyond the ring), compiled apart from the
+// others (moe_layer_tk*_kp.cu) so that their code does not share a module
+// with the instantiations that never need it.
+template <int MC_GU, int MC_D, int TK, bool GV, bool TL, int FMT = 0, bool KP = false>
 __global__ void __launch_bounds__(kLayerThreads, 1) moe_layer_kernel(const LayerParams p) {
     static_assert(FMT == 0 || (!GV && !TL), "GEMV variant and t layout: NVFP4 experts only");
-    constexpr bool kDownParts = down_parts_possible(FMT, MC_D);
+    static_assert(!KP || down_parts_possible(FMT, MC_D), "K-parts: FP8 / BF16 with enough chunks per warp");
+    constexpr bool kDownParts = KP;
     // one-row form with 4 chunks per warp (hidden 3200 .. 4096, a ring of 5
     // to 7 slots): each unit's gate slot is released before its up slot is
     // waited for, which keeps one more slot in flight; the other
@@ -1397,6 +1401,30 @@ void *layer_kernel_table(int mc_gu, int mc_d) {
          (void *)moe_layer_kernel<4, 3, TK, GV, false, FMT>, (void *)moe_layer_kernel<4, 4, TK, GV, false, FMT>}};
     if (mc_gu < 1 || mc_gu > 4 || mc_d < 1 || mc_d > 4) return nullptr;
     return tab[mc_gu - 1][mc_d - 1];
+}
+
+// The K-part instantiations of one top-k class and expert format: MC_GU
+// 1..4 x MC_D 2..4, those that down_parts_possible allows (null otherwise).
+template <int MC_GU, int MC_D, int TK, int FMT>
+void *layer_kernel_kp_entry() {
+    if constexpr (down_parts_possible(FMT, MC_D))
+        return (void *)moe_layer_kernel<MC_GU, MC_D, TK, false, false, FMT, true>;
+    else
+        return nullptr;
+}
+template <int TK, int FMT>
+void *layer_kernel_kp_table(int mc_gu, int mc_d) {
+    static void *const tab[4][3] = {
+        {layer_kernel_kp_entry<1, 2, TK, FMT>(), layer_kernel_kp_entry<1, 3, TK, FMT>(),
+         layer_kernel_kp_entry<1, 4, TK, FMT>()},
+        {layer_kernel_kp_entry<2, 2, TK, FMT>(), layer_kernel_kp_entry<2, 3, TK, FMT>(),
+         layer_kernel_kp_entry<2, 4, TK, FMT>()},
+        {layer_kernel_kp_entry<3, 2, TK, FMT>(), layer_kernel_kp_entry<3, 3, TK, FMT>(),
+         layer_kernel_kp_entry<3, 4, TK, FMT>()},
+        {layer_kernel_kp_entry<4, 2, TK, FMT>(), layer_kernel_kp_entry<4, 3, TK, FMT>(),
+         layer_kernel_kp_entry<4, 4, TK, FMT>()}};
+    if (mc_gu < 1 || mc_gu > 4 || mc_d < 2 || mc_d > 4) return nullptr;
+    return tab[mc_gu - 1][mc_d - 2];
 }
 
 // The t-layout (fused one-row) instantiations of one top-k class: MC_GU
